@@ -1,0 +1,159 @@
+"""ctypes binding of ``include/gemm_f16.h`` (argument marshalling only).
+
+Every function here forwards to the C-ABI library ``libgemm_f16.so``; the
+arithmetic runs in its CUDA kernels. Torch is used for device memory and the
+current stream. If the library has not been built, every call raises
+``GemmError`` — there is no fallback path.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libgemm_f16.so"
+
+SCHED_GROUPED = 0x1
+SCHED_CROSS_TILE = 0x2
+
+_STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
+           3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT"}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        name = _STATUS.get(self.status, f"status {status}")
+        super().__init__(f"{what}: {name}" if what else name)
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load_library():
+    """Load (once) and return the ctypes handle of libgemm_f16.so."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise GemmError(3, f"{path} is missing: build it with "
+                           "`python -m dense_gemm_gb300.build` (no fallback path exists)")
+    lib = ctypes.CDLL(path)
+    i64, i32, u32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p
+    pi32 = ctypes.POINTER(ctypes.c_int32)
+    lib.gemm_f16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                             i32, u32, vp]
+    lib.gemm_f16.restype = ctypes.c_int
+    lib.gemm_f16_tile_map.argtypes = [i32, i32, i32, u32, i32, vp, vp]
+    lib.gemm_f16_tile_map.restype = ctypes.c_int
+    lib.gemm_f16_get_config.argtypes = [i64, i64, pi32, pi32, pi32, pi32, pi32]
+    lib.gemm_f16_get_config.restype = ctypes.c_int
+    lib.gemm_f16_kernel_info.argtypes = [i32, pi32, pi32, pi32, pi32]
+    lib.gemm_f16_kernel_info.restype = ctypes.c_int
+    lib.gemm_f16_sync_status.argtypes = [vp]
+    lib.gemm_f16_sync_status.restype = ctypes.c_int
+    lib.gemm_f16_set_wait_timeout.argtypes = [ctypes.c_uint64]
+    lib.gemm_f16_set_wait_timeout.restype = ctypes.c_int
+    lib.gemm_f16_status_str.argtypes = [ctypes.c_int]
+    lib.gemm_f16_status_str.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise GemmError(status, what)
+
+
+def _stream_handle(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def status_str(status: int) -> str:
+    return load_library().gemm_f16_status_str(int(status)).decode()
+
+
+def gemm_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int,
+             stride_am: int, stride_ak: int, stride_bk: int, stride_bn: int,
+             stride_cm: int, stride_cn: int, group_size_m: int = 8,
+             schedule_flags: int = SCHED_GROUPED | SCHED_CROSS_TILE, stream: int = 0) -> int:
+    """The C call with raw integers; returns the status code (no raise)."""
+    return load_library().gemm_f16(A_ptr, B_ptr, C_ptr, M, N, K, stride_am, stride_ak,
+                                   stride_bk, stride_bn, stride_cm, stride_cn,
+                                   group_size_m, schedule_flags, stream)
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
+         group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
+         stream=None) -> torch.Tensor:
+    """C = A @ B with A [M,K], B [K,N] fp16 CUDA tensors; C fp32 [M,N].
+
+    ``out`` (fp32, [M,N], unit column stride) is written if given, else
+    allocated. Strided views are passed through as strides.
+    """
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shapes {tuple(A.shape)} @ {tuple(B.shape)} do not chain")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, K = A.shape
+    N = B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
+        raise ValueError("out must be a float32 CUDA tensor of shape [M, N]")
+    flags = (SCHED_GROUPED if grouped else 0) | (SCHED_CROSS_TILE if cross_tile else 0)
+    sam, sak = A.stride()
+    sbk, sbn = B.stride()
+    scm, scn = out.stride()
+    # torch gives stride 1 to size-1 dims' neighbours freely; keep them >= 1
+    st = gemm_raw(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
+                  max(sam, 1), max(sak, 1), max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1),
+                  group_size_m, flags, _stream_handle(stream))
+    _check(st, "gemm_f16")
+    return out
+
+
+def tile_map(num_m_tiles: int, num_n_tiles: int, group_size_m: int, grouped: bool,
+             grid: int, device=None, stream=None) -> torch.Tensor:
+    """[T, 3] int32 CUDA tensor from the kernel's scheduler: row tile_id =
+    (program id, tile_m, tile_n)."""
+    device = device or torch.device("cuda")
+    out = torch.full((num_m_tiles * num_n_tiles, 3), -1, dtype=torch.int32, device=device)
+    st = load_library().gemm_f16_tile_map(num_m_tiles, num_n_tiles, group_size_m,
+                                          SCHED_GROUPED if grouped else 0, grid,
+                                          out.data_ptr(), _stream_handle(stream))
+    _check(st, "gemm_f16_tile_map")
+    return out
+
+
+def get_config(M: int = 0, N: int = 0) -> dict:
+    v = [ctypes.c_int32() for _ in range(5)]
+    _check(load_library().gemm_f16_get_config(M, N, *[ctypes.byref(x) for x in v]),
+           "gemm_f16_get_config")
+    return dict(zip(("bm", "bn", "bk", "stages", "grid"), (x.value for x in v)))
+
+
+def kernel_info(variant: int = 0) -> dict:
+    v = [ctypes.c_int32() for _ in range(4)]
+    _check(load_library().gemm_f16_kernel_info(variant, *[ctypes.byref(x) for x in v]),
+           "gemm_f16_kernel_info")
+    return dict(zip(("regs_per_thread", "static_smem", "dynamic_smem", "threads_per_cta"),
+                    (x.value for x in v)))
+
+
+def sync_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status code."""
+    return int(load_library().gemm_f16_sync_status(_stream_handle(stream)))
+
+
+def set_wait_timeout(ns: int):
+    _check(load_library().gemm_f16_set_wait_timeout(int(ns)), "gemm_f16_set_wait_timeout")

@@ -1,0 +1,153 @@
+/*
+ * gemm_f16 — persistent FP16 GEMM for GB300 (sm_103a), C ABI.
+ *
+ *   C[M,N] = A[M,K] @ B[K,N]   fp16 inputs, fp32 accumulation, fp32 output.
+ *
+ * The operation and its scheduling follow four pages:
+ *  [persistent] "(1/n) Triton matmul 커널 탐험 - persistent kernel은 그 자체로
+ *               빠르지 않다": sections "naive tiled matmul" (masked tile GEMM,
+ *               FP32 accumulator from zero, C stored, never read),
+ *               "naive persistent matmul" (grid = min(#SMs, #tiles); program
+ *               pid visits tile_id = pid, pid + grid, ...).
+ *  [swizzle]    "(2/n) Triton matmul 커널 탐험 - grouped ordering(CTA swizzle)도
+ *               늘 빠르게 만들지는 않는다": section "구현" (grouped tile order).
+ *  [flatten]    "(3/n) Triton matmul 커널 탐험 - cross tile pipelining 적용":
+ *               one flattened (tile, k) loop so the next tile's loads overlap
+ *               the current tile's store.
+ *  [roofline]   "4주차 정리: Roofline과 Tiling": section 5 (FLOPs = 2MNK).
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers to matrices are DEVICE pointers owned by the caller. The
+ *    library allocates no device memory per call; its only device state is a
+ *    few status words in the library image (one copy per device).
+ *  - Strides are in ELEMENTS, as in the pages' kernels
+ *    (stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn):
+ *    A(i,k) = A[i*stride_am + k*stride_ak], B(k,j) = B[k*stride_bk + j*stride_bn],
+ *    C(i,j) = C[i*stride_cm + j*stride_cn].
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *    call returns without waiting. Launch errors are returned; errors raised
+ *    while the kernel runs (a bounded wait that ran out) are reported by
+ *    gemm_f16_sync_status().
+ *  - Every entry point validates its arguments before touching the GPU and
+ *    returns GEMM_ERR_INVALID_ARG / GEMM_ERR_UNSUPPORTED without side effects.
+ *  - Thread safety: calls from several host threads are allowed; calls that
+ *    overlap on the GPU and write the same C race (the caller's problem).
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride/flag/G */
+    GEMM_ERR_UNSUPPORTED = 2, /* layout the kernels do not take (see gemm_f16) */
+    GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed            */
+    GEMM_ERR_TIMEOUT = 4      /* a bounded device wait ran out (kernel gave up) */
+} gemm_status_t;
+
+/* schedule_flags bits */
+#define GEMM_SCHED_GROUPED 0x1u    /* grouped ("CTA swizzle") tile order; else row-major */
+#define GEMM_SCHED_CROSS_TILE 0x2u /* overlap the next tile's loads/MMAs with the current
+                                      tile's epilogue; else drain at every tile boundary */
+#define GEMM_SCHED_ALL_FLAGS 0x3u
+
+/*
+ * gemm_f16 — C = A @ B.
+ *
+ * Defined by [persistent] "naive tiled matmul" / "naive persistent matmul",
+ * the tile order by [swizzle] "구현", the cross-tile overlap by [flatten].
+ *
+ * A: __half[M,K] (device), B: __half[K,N] (device), C: float[M,N] (device).
+ * C is overwritten and never read; it must not overlap A or B (undefined).
+ * group_size_m: GROUP_SIZE_M of the grouped order, >= 1 when
+ *   GEMM_SCHED_GROUPED is set (ignored otherwise; G >= #m-tiles gives one
+ *   group, G == 1 gives the row-major order).
+ * schedule_flags: OR of GEMM_SCHED_* bits; any other bit -> INVALID_ARG.
+ *
+ * Layouts taken: A with stride_ak == 1 (K-major) or stride_am == 1 (M-major);
+ * B with stride_bk == 1 (K-major) or stride_bn == 1 (N-major); C with
+ * stride_cn == 1. Other layouts -> GEMM_ERR_UNSUPPORTED. All strides >= 1.
+ * Operands whose base address is 16-byte aligned and whose non-unit stride is
+ * a multiple of 8 elements (A, B) or 4 elements (C) go through TMA; others
+ * (e.g. K = 257 row-major) through a predicated load/store path with the same
+ * results.
+ * Sizes: M, N, K >= 0, each < 2^31. M == 0 or N == 0: nothing is done.
+ * K == 0: C is set to 0.
+ * Returns GEMM_OK once the work is enqueued.
+ */
+gemm_status_t gemm_f16(const void *A, const void *B, float *C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t stride_am, int64_t stride_ak,
+                       int64_t stride_bk, int64_t stride_bn,
+                       int64_t stride_cm, int64_t stride_cn,
+                       int32_t group_size_m, uint32_t schedule_flags,
+                       gemm_stream_t stream);
+
+/*
+ * gemm_f16_tile_map — the kernel's own tile scheduler, run on the GPU.
+ *
+ * Defined by [persistent] "naive persistent matmul" (visiting order) and
+ * [swizzle] "구현" (grouped map) / [persistent] "naive tiled matmul"
+ * (row-major map). Uses the same device function as gemm_f16.
+ * out_dev: int32[num_m_tiles*num_n_tiles][3] (device, caller-owned); row
+ * tile_id receives {program id that processes it, tile_m, tile_n} where
+ * program p visits tile_id = p, p + grid, p + 2*grid, ...
+ * grid >= 1; num_m_tiles, num_n_tiles >= 1 and their product < 2^31;
+ * flags: only GEMM_SCHED_GROUPED matters (others allowed).
+ */
+gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles,
+                                int32_t group_size_m, uint32_t flags, int32_t grid,
+                                int32_t *out_dev, gemm_stream_t stream);
+
+/*
+ * gemm_f16_get_config — tile shape and launch size of gemm_f16 for an M x N
+ * output on the current device. Any output pointer may be NULL.
+ * bm, bn, bk: CTA tile; stages: shared-memory ring depth; grid: persistent
+ * CTAs = min(#SMs, cdiv(M,bm)*cdiv(N,bn)) (needs a device; set to 0 when
+ * M or N is 0).
+ */
+gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn,
+                                  int32_t *bk, int32_t *stages, int32_t *grid);
+
+/*
+ * gemm_f16_kernel_info — compiled resource use of a kernel variant
+ * (cudaFuncGetAttributes): variant 0 = TMA loads + TMA store, 1 = TMA loads +
+ * predicated store, 2 = predicated loads + TMA store, 3 = predicated loads +
+ * predicated store. Outputs may be NULL. Needs a device.
+ */
+gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
+                                   int32_t *static_smem, int32_t *dynamic_smem,
+                                   int32_t *threads_per_cta);
+
+/*
+ * gemm_f16_sync_status — synchronize `stream`, then return and clear the
+ * sticky device status of the current device: GEMM_ERR_TIMEOUT if any
+ * kernel's bounded wait ran out since the last call (that call's C is
+ * undefined), GEMM_ERR_CUDA if the synchronize failed, else GEMM_OK.
+ */
+gemm_status_t gemm_f16_sync_status(gemm_stream_t stream);
+
+/*
+ * gemm_f16_set_wait_timeout — upper bound, in nanoseconds of GPU global
+ * time, on any single wait inside the kernels (default 2e9 = 2 s). Applies
+ * to launches enqueued after the call. ns must be >= 1000.
+ */
+gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns);
+
+/* gemm_f16_status_str — static, human-readable name of a status code. */
+const char *gemm_f16_status_str(gemm_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */
