@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Benchmark of the persistent FP16 GEMM (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gemm_f16|reference]
+                    [--workload NAME] [--order grouped|row-major] [--cross-tile on|off]
+
+A step is one gemm_f16 call (one persistent kernel launch) over the whole
+workload; the default workload is M = N = 16384, K = 4096, A and B row-major
+fp16 N(0,1), fp32 accumulate and output, grouped order with GROUP_SIZE_M = 8,
+cross-tile pipelining on. ``value`` is the device-timed throughput (CUDA
+events on the launching stream, inputs resident in HBM); ``e2e`` is the same
+metric through ``gemm_from_host`` with pinned host operands, host<->device
+copies inside the timed region. Under torchrun every rank runs its own copy
+of the workload on its own GPU (independent problems, weak scaling).
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on
+a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+NOMINAL_FP16_TFLOPS = 2250.0        # nominal dense bf16/fp16 tensor peak per GPU
+NVL72_SPEC_FP16_TFLOPS = 2500.0     # GB300 NVL72 dense fp16 (360 PF sparse / 72 / 2)
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=500)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["gemm_f16", "reference"], default="gemm_f16")
+    p.add_argument("--workload", default=None)
+    p.add_argument("--order", choices=["grouped", "row-major"], default="grouped")
+    p.add_argument("--group-size", type=int, default=8)
+    p.add_argument("--cross-tile", choices=["on", "off"], default="on")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="approximate CPU time of the oracle sample")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("dense_gemm_gb300/csrc/gemm_kernel.cuh", "dense_gemm_gb300/csrc/ptx.cuh",
+                "dense_gemm_gb300/csrc/gemm_f16.cu"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload_name, order, cross):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source for this workload and schedule; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = f"{workload_name}|{order}|cross={'on' if cross else 'off'}"
+    e = d.get(key)
+    if not e or e.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples with host timestamps."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None, period_ms=100):
+        self.samples = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if gpu_id:
+            cmd += ["-i", str(gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        used = inside
+        if not used:  # timed region shorter than the sampling period: nearest samples
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            used = [s for _, s in near[:2]]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [num(s[1]) for s in used if num(s[1]) is not None]
+        smax = [num(s[2]) for s in used if num(s[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in used for i in range(4) if s[5 + i].lower() == "active"})
+        power = [num(s[3]) for s in used if num(s[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons,
+                "power_w_max": max(power) if power else None,
+                "samples": len(inside), "samples_near": len(used) - len(inside)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def l2_note(w):
+    total = 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
+    if total > 126 * 2 ** 20:
+        return f"no flush: A+B+C = {total / 2 ** 30:.2f} GiB per step, larger than the 126 MiB L2"
+    return f"L2-resident: A+B+C = {total / 2 ** 20:.1f} MiB per step (smaller than L2, no flush)"
+
+
+def workload_config(w, args, extra=None):
+    cfg = {"workload": w.describe(), "name": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "order": args.order, "group_size_m": args.group_size if args.order == "grouped" else None,
+           "cross_tile": args.cross_tile == "on", "a_layout": w.a_layout, "b_layout": w.b_layout,
+           "values": w.dist, "seed": w.seed,
+           "l2": l2_note(w)}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------- CPU oracle legs
+
+def oracle_rows_timing(A, B, rows, threads):
+    import numpy as np
+    import oracle
+    r = np.asarray(rows, dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.gemm_rows(A, B, rows=r, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(A, B, seconds):
+    """Time the oracle, as it stands, on a bounded sample of whole C rows."""
+    import numpy as np
+    import oracle
+    threads = os.cpu_count() or 1
+    M, K = A.shape
+    N = B.shape[1]
+    rng = np.random.default_rng(0)
+    probe = max(threads, 4)
+    t_probe = oracle_rows_timing(A, B, rng.integers(0, M, probe), threads)
+    rows = int(max(probe, min(M, probe * seconds / max(t_probe, 1e-6))))
+    sample = rng.integers(0, M, rows)
+    t = oracle_rows_timing(A, B, sample, threads)
+    flops = 2.0 * rows * N * K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": int(oracle.max_threads()),
+            "kind": "oracle",
+            "sample": f"{rows} random rows of C (full N={N}, K={K}) = {rows / M:.4%} of the "
+                      f"workload's FLOPs, {t:.1f} s on {threads} host threads"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    A, B = w.operands()
+    threads = os.cpu_count() or 1
+    M, K = A.shape
+    N = B.shape[1]
+    rng = np.random.default_rng(1)
+    probe = max(threads, 4)
+    t_probe = oracle_rows_timing(A, B, rng.integers(0, M, probe), threads)
+    per_step_s = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(M, probe * per_step_s / max(t_probe, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_rows_timing(A, B, rng.integers(0, M, rows), threads)
+    times = [oracle_rows_timing(A, B, rng.integers(0, M, rows), threads) for _ in range(args.steps)]
+    total = sum(times)
+    flops_step = 2.0 * rows * N * K
+    value = flops_step * args.steps / total / 1e12
+    line = {
+        "impl": "reference", "metric": "FP16 GEMM TFLOPS (2MNK/s)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, args, {"rows_per_step": rows}),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
+                         "cores": int(oracle.max_threads()),
+                         "sample": f"each step: {rows} random whole rows of C "
+                                   f"({rows / M:.4%} of the workload)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU leg
+
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from dense_gemm_gb300 import gemm, gemm_from_host, kernel_info, sync_status
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    grouped = args.order == "grouped"
+    cross = args.cross_tile == "on"
+    A_host, B_host = w.operands()
+    A = A_host.to(dev)
+    B = B_host.to(dev)
+    C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        gemm(A, B, C, group_size_m=args.group_size, grouped=grouped, cross_tile=cross,
+             stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if sync_status(stream) != 0:
+        raise RuntimeError("device status after warm-up is not GEMM_OK")
+
+    sampler = None
+    if not args.no_clocks:
+        props = torch.cuda.get_device_properties(dev)
+        gpu_id = getattr(props, "uuid", None)
+        gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
+        sampler = ClockSampler(gpu_id)
+        time.sleep(0.6)   # let nvidia-smi start
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize(dev)
+
+    K_steps = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K_steps + 1)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev[0].record(stream)
+    for i in range(K_steps):
+        step()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    status = sync_status(stream)
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K_steps)]
+    total_ms = ev[0].elapsed_time(ev[K_steps])
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    flops = 2.0 * w.M * w.N * w.K
+    value = world * flops * K_steps / (total_ms * 1e-3) / 1e12
+    avg_launch_ms = statistics.mean(per_launch_ms)
+    med_launch_ms = statistics.median(per_launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+
+    # ---- end to end: host operands, copies in the timed region
+    e2e = None
+    if not args.no_e2e and args.e2e_steps > 0:
+        A_pin = A_host.pin_memory()
+        B_pin = B_host.pin_memory()
+        C_pin = torch.empty((w.M, w.N), dtype=torch.float32, pin_memory=True)
+        ws = (torch.empty_strided(A.shape, A.stride(), dtype=A.dtype, device=dev),
+              torch.empty_strided(B.shape, B.stride(), dtype=B.dtype, device=dev), C)
+        gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
+                       grouped=grouped, cross_tile=cross, stream=stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
+                           grouped=grouped, cross_tile=cross, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        in_bytes = A_host.untyped_storage().nbytes() + B_host.untyped_storage().nbytes()
+        e2e = {"value": world * flops * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * w.M * w.N,
+               "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
+               "api": "dense_gemm_gb300.gemm_from_host (pinned host A, B, C)"}
+        del A_pin, B_pin, C_pin
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    compulsory = 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
+    intensity = flops / compulsory
+    bound_tflops = min(NVL72_SPEC_FP16_TFLOPS, hbm * 1e9 * intensity / 1e12)
+    traffic = recorded_traffic(w.name, args.order, cross)
+    info = kernel_info(0)
+
+    line = {
+        "metric": "FP16 GEMM TFLOPS (2MNK/s) and % of GB300 dense FP16 peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K_steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / K_steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(w, args, {"parallelism": f"independent replicas x{world}",
+                                            "accumulate": "f32", "output": "f32"}),
+        "pct_of_peak": {"nvl72_spec_2500": 100.0 * value / world / NVL72_SPEC_FP16_TFLOPS,
+                        "nominal_2250": 100.0 * value / world / NOMINAL_FP16_TFLOPS,
+                        f"{peak_src}_bf16_{peak:g}": 100.0 * value / world / peak},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} cuBLAS bf16 burst (MEASURED_PEAKS.json) x nominal "
+                                    "fp16/bf16 ratio 1.0",
+                     "kernel": "g16::gemm_f16_persistent<true,true>",
+                     "algorithmic_flops_per_launch": flops,
+                     "avg_launch_ms": avg_launch_ms, "median_launch_ms": med_launch_ms,
+                     "workload_roofline_tflops_min_P_BWxI": bound_tflops,
+                     "compulsory_bytes": compulsory},
+        "e2e": e2e,
+        "gpu_launches": K_steps,
+        "clocks": clocks,
+        "kernel_resources": info,
+        "device_status": status,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(A_host, B_host, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0 if status == 0 else 1
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

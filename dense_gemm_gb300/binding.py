@@ -157,3 +157,32 @@ def sync_status(stream=None) -> int:
 
 def set_wait_timeout(ns: int):
     _check(load_library().gemm_f16_set_wait_timeout(int(ns)), "gemm_f16_set_wait_timeout")
+
+
+def gemm_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Tensor = None, *,
+                   workspace=None, group_size_m: int = 8, grouped: bool = True,
+                   cross_tile: bool = True, stream=None) -> torch.Tensor:
+    """End-to-end call on HOST operands: copy A and B (pinned host fp16) to the
+    device, run gemm_f16, copy C back into ``C_host`` (pinned fp32).
+
+    ``workspace`` = (A_dev, B_dev, C_dev) device buffers of matching shapes to
+    reuse across calls; allocated when omitted. Copies and the kernel are
+    enqueued on one stream; the call returns after the device-to-host copy has
+    been enqueued (synchronize the stream before reading ``C_host``).
+    """
+    M, K = A_host.shape
+    N = B_host.shape[1]
+    if C_host is None:
+        C_host = torch.empty((M, N), dtype=torch.float32, pin_memory=True)
+    if workspace is None:
+        workspace = (torch.empty_like(A_host, device="cuda"), torch.empty_like(B_host, device="cuda"),
+                     torch.empty((M, N), dtype=torch.float32, device="cuda"))
+    A_dev, B_dev, C_dev = workspace
+    s = stream if stream is not None else torch.cuda.current_stream()
+    with torch.cuda.stream(s):
+        A_dev.copy_(A_host, non_blocking=True)
+        B_dev.copy_(B_host, non_blocking=True)
+        gemm(A_dev, B_dev, C_dev, group_size_m=group_size_m, grouped=grouped,
+             cross_tile=cross_tile, stream=s)
+        C_host.copy_(C_dev, non_blocking=True)
+    return C_host

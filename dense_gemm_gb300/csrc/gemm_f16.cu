@@ -1,0 +1,318 @@
+// Host side of the gemm_f16 C ABI (declared in include/gemm_f16.h): argument
+// validation, layout/path selection, TMA tensor-map encoding and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using namespace g16;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<uint32_t> g_epoch{0};
+
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_err = cudaSuccess;
+    int num_sms = 0;
+};
+DeviceState g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+bool log_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("GEMM_LOG");
+        return e != nullptr && e[0] != '\0' && e[0] != '0';
+    }();
+    return on;
+}
+
+template <bool L, bool S>
+cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(gemm_f16_persistent<L, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SMEM_BYTES);
+}
+
+cudaError_t device_init(int dev, DeviceState **out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceState &d = g_dev[dev];
+    std::call_once(d.once, [&d, dev] {
+        cudaError_t e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = set_smem_attr<true, true>();
+        if (e == cudaSuccess) e = set_smem_attr<true, false>();
+        if (e == cudaSuccess) e = set_smem_attr<false, true>();
+        if (e == cudaSuccess) e = set_smem_attr<false, false>();
+        d.init_err = e;
+    });
+    *out = &d;
+    return d.init_err;
+}
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+// 2-D tiled tensor map, inner dimension first, 128-byte swizzle, OOB -> zero.
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {outer_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// TMA can describe an operand whose contiguous extent is `inner` and whose other
+// stride is `outer_stride` elements of `esize` bytes.
+bool tma_ok(const void *p, int64_t inner, int64_t outer_stride, int esize) {
+    return aligned16(p) && (outer_stride * esize) % 16 == 0 && outer_stride >= inner &&
+           outer_stride * esize < (int64_t(1) << 40);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <bool L, bool S>
+cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
+                   int grid, cudaStream_t stream) {
+    gemm_f16_persistent<L, S><<<grid, cta_threads(L), SMEM_BYTES, stream>>>(a, b, c, p);
+    return cudaGetLastError();
+}
+
+uint32_t next_epoch() {
+    uint32_t e = g_epoch.fetch_add(1) + 1;
+    if (e == 0) e = g_epoch.fetch_add(1) + 1;  // 0 means "no abort"
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gemm_f16_status_str(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns) {
+    if (ns < 1000) return GEMM_ERR_INVALID_ARG;
+    g_timeout_ns.store(ns);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                       int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                       int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
+                       uint32_t schedule_flags, gemm_stream_t stream_) {
+    // ---- validation (no GPU work before this point)
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
+        return GEMM_ERR_INVALID_ARG;
+    if (stride_am < 1 || stride_ak < 1 || stride_bk < 1 || stride_bn < 1 || stride_cm < 1 ||
+        stride_cn < 1)
+        return GEMM_ERR_INVALID_ARG;
+    if (schedule_flags & ~GEMM_SCHED_ALL_FLAGS) return GEMM_ERR_INVALID_ARG;
+    const bool grouped = (schedule_flags & GEMM_SCHED_GROUPED) != 0;
+    if (grouped && group_size_m < 1) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return GEMM_ERR_INVALID_ARG;
+    if (stride_cn != 1) return GEMM_ERR_UNSUPPORTED;
+    if (M > 1 && stride_cm < N) return GEMM_ERR_INVALID_ARG;  // C rows would overlap
+
+    const bool a_k = stride_ak == 1, a_m = !a_k && stride_am == 1;
+    const bool b_n = stride_bn == 1, b_k = !b_n && stride_bk == 1;
+    if (K > 0 && (!(a_k || a_m) || !(b_n || b_k))) return GEMM_ERR_UNSUPPORTED;
+
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GEMM_ERR_CUDA;
+    DeviceState *ds = nullptr;
+    if (device_init(dev, &ds) != cudaSuccess) return GEMM_ERR_CUDA;
+
+    if (K == 0) {
+        const int64_t total = M * N;
+        const int threads = 256;
+        const int64_t blocks64 = cdiv(total, threads);
+        const int blocks = int(blocks64 < 8 * int64_t(ds->num_sms) ? blocks64 : 8 * int64_t(ds->num_sms));
+        zero_c_kernel<<<blocks, threads, 0, stream>>>(C, M, N, stride_cm);
+        return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    const int64_t nm = cdiv(M, BM), nn = cdiv(N, BN);
+    if (nm * nn > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+
+    // ---- path selection per tensor
+    const bool a_tma = a_k ? tma_ok(A, K, stride_am, 2) : tma_ok(A, M, stride_ak, 2);
+    const bool b_tma = b_n ? tma_ok(B, N, stride_bk, 2) : tma_ok(B, K, stride_bn, 2);
+    const bool load_tma = a_tma && b_tma;
+    const bool store_tma = tma_ok(C, N, stride_cm, 4);
+
+    CUtensorMap tmA, tmB, tmC;
+    std::memset(&tmA, 0, sizeof(tmA));
+    std::memset(&tmB, 0, sizeof(tmB));
+    std::memset(&tmC, 0, sizeof(tmC));
+    if (load_tma) {
+        const bool okA = a_k ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, stride_am * 2, BK, BM)
+                             : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, M, K, stride_ak * 2,
+                                         MN_CHUNK, BK);
+        const bool okB = b_k ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, stride_bn * 2, BK, BN)
+                             : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, stride_bk * 2,
+                                         MN_CHUNK, BK);
+        if (!okA || !okB) return GEMM_ERR_CUDA;
+    }
+    if (store_tma) {
+        if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, stride_cm * 4, EPI_COLS, 32))
+            return GEMM_ERR_CUDA;
+    }
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.A = static_cast<const uint16_t *>(A);
+    p.B = static_cast<const uint16_t *>(B);
+    p.C = C;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.sam = stride_am;
+    p.sak = stride_ak;
+    p.sbk = stride_bk;
+    p.sbn = stride_bn;
+    p.scm = stride_cm;
+    p.sched.nm = int32_t(nm);
+    p.sched.nn = int32_t(nn);
+    p.sched.group_m = grouped ? group_size_m : 1;
+    p.sched.grouped = grouped ? 1 : 0;
+    p.num_tiles = int32_t(nm * nn);
+    p.num_kb = int32_t(cdiv(K, BK));
+    p.a_mn = a_k ? 0u : 1u;
+    p.b_mn = b_n ? 1u : 0u;
+    p.idesc = make_idesc(p.a_mn, p.b_mn);
+    p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
+    p.wait.timeout_ns = g_timeout_ns.load();
+    p.wait.epoch = next_epoch();
+
+    const int grid = int(p.num_tiles < ds->num_sms ? p.num_tiles : ds->num_sms);
+    if (log_enabled())
+        std::fprintf(stderr,
+                     "[gemm_f16] M=%lld N=%lld K=%lld tiles=%d grid=%d load=%s store=%s A=%s B=%s "
+                     "order=%s G=%d cross_tile=%u\n",
+                     (long long)M, (long long)N, (long long)K, p.num_tiles, grid,
+                     load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
+                     p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
+                     grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile);
+
+    cudaError_t e;
+    if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, grid, stream);
+    else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, grid, stream);
+    else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, grid, stream);
+    else e = launch<false, false>(tmA, tmB, tmC, p, grid, stream);
+    return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles, int32_t group_size_m,
+                                uint32_t flags, int32_t grid, int32_t *out_dev,
+                                gemm_stream_t stream_) {
+    if (num_m_tiles < 1 || num_n_tiles < 1 || grid < 1 || out_dev == nullptr)
+        return GEMM_ERR_INVALID_ARG;
+    if (int64_t(num_m_tiles) * num_n_tiles > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    const bool grouped = (flags & GEMM_SCHED_GROUPED) != 0;
+    if (grouped && group_size_m < 1) return GEMM_ERR_INVALID_ARG;
+    Sched s;
+    s.nm = num_m_tiles;
+    s.nn = num_n_tiles;
+    s.group_m = grouped ? group_size_m : 1;
+    s.grouped = grouped ? 1 : 0;
+    tile_map_kernel<<<grid, 32, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(
+        s, num_m_tiles * num_n_tiles, out_dev);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn, int32_t *bk,
+                                  int32_t *stages, int32_t *grid) {
+    if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    if (bm) *bm = BM;
+    if (bn) *bn = BN;
+    if (bk) *bk = BK;
+    if (stages) *stages = STAGES;
+    if (grid) {
+        *grid = 0;
+        if (M > 0 && N > 0) {
+            int dev = 0;
+            DeviceState *ds = nullptr;
+            if (cudaGetDevice(&dev) != cudaSuccess || device_init(dev, &ds) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+            const int64_t tiles = cdiv(M, BM) * cdiv(N, BN);
+            *grid = int32_t(tiles < ds->num_sms ? tiles : ds->num_sms);
+        }
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
+                                   int32_t *dynamic_smem, int32_t *threads) {
+    if (variant < 0 || variant > 3) return GEMM_ERR_INVALID_ARG;
+    cudaFuncAttributes a;
+    cudaError_t e;
+    int thr;
+    switch (variant) {
+        case 0: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, true>); thr = cta_threads(true); break;
+        case 1: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, false>); thr = cta_threads(true); break;
+        case 2: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, true>); thr = cta_threads(false); break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, false>); thr = cta_threads(false); break;
+    }
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    if (regs) *regs = a.numRegs;
+    if (static_smem) *static_smem = int32_t(a.sharedSizeBytes);
+    if (dynamic_smem) *dynamic_smem = SMEM_BYTES;
+    if (threads) *threads = thr;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_sync_status(gemm_stream_t stream_) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    unsigned int st = 0;
+    const unsigned int zero = 0;
+    if (cudaMemcpyFromSymbol(&st, g_status, sizeof(st)) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (st != 0 && cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return st == 0 ? GEMM_OK : static_cast<gemm_status_t>(st);
+}
+
+}  // extern "C"

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Bar: tile map and integer-valued inputs bit-exact; random fp16 inputs within
+max|C - C_ref| <= 2e-3 sqrt(K) max|A| max|B| and relative Frobenius error
+<= 1e-3, on every element at small sizes and on sampled tiles plus row/column
+sum identities at the full workload sizes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_gemm_gb300 import GemmError, gemm, get_config, sync_status, tile_map, kernel_info
+from dense_gemm_gb300.inputs import WORKLOADS, draw, relayout
+from gpu_util import (assert_within_bound, check_row_col_sums, check_sampled_tiles, require_gpu,
+                      run, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+    from dense_gemm_gb300 import build
+    build.build()
+    torch.cuda.init()
+    yield
+    assert sync_status() == 0
+
+
+ORDERS = [(True, True), (True, False), (False, True), (False, False)]  # (grouped, cross_tile)
+
+
+# ------------------------------------------------------------------ tile map
+
+@pytest.mark.parametrize("nm,nn,G,grid", [(1, 1, 8, 1), (3, 2, 2, 4), (64, 32, 8, 152),
+                                          (128, 64, 8, 152), (65, 63, 8, 152), (37, 13, 5, 7),
+                                          (7, 40, 12, 300), (1, 1000, 8, 152), (1000, 1, 8, 152),
+                                          (64, 64, 1, 152), (9, 9, 100, 2)])
+@pytest.mark.parametrize("grouped", [True, False])
+def test_tile_map_bit_exact(nm, nn, G, grid, grouped):
+    got = tile_map(nm, nn, G, grouped, grid).cpu().numpy()
+    want = oracle.schedule(nm, nn, G, grouped, grid)
+    assert np.array_equal(got, want)
+
+
+# ------------------------------------------------------------------ exact (integer) parity
+
+SMALL_SHAPES = [(1, 1, 1), (128, 256, 64), (129, 257, 65), (300, 600, 200), (64, 100, 1000),
+                (256, 512, 128), (7, 1000, 33), (1000, 9, 70), (640, 640, 640)]
+
+
+@pytest.mark.parametrize("shape", SMALL_SHAPES)
+@pytest.mark.parametrize("grouped,cross", ORDERS)
+def test_integer_inputs_bit_exact(shape, grouped, cross):
+    M, N, K = shape
+    A = draw(M, K, "int", 7 + M)
+    B = draw(K, N, "int", 8 + N)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross, G=3)
+    assert np.array_equal(C, oracle.gemm(A, B))
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [("row", "row"), ("row", "col"), ("col", "row"),
+                                               ("col", "col")])
+@pytest.mark.parametrize("shape", [(200, 300, 136), (384, 512, 256), (130, 260, 72)])
+def test_operand_layouts_bit_exact(a_layout, b_layout, shape):
+    M, N, K = shape
+    A = draw(M, K, "int", 11)
+    B = draw(K, N, "int", 12)
+    ref = oracle.gemm(A, B)
+    _, C = run(relayout(A, a_layout), relayout(B, b_layout))
+    assert np.array_equal(C, ref)
+
+
+# ------------------------------------------------------------------ random parity, every element
+
+@pytest.mark.parametrize("shape", [(512, 512, 512), (300, 600, 200), (1000, 1000, 1000),
+                                   (128, 2048, 4096), (2176, 384, 320)])
+@pytest.mark.parametrize("dist", ["uniform", "normal"])
+def test_random_inputs_within_bound(shape, dist):
+    M, N, K = shape
+    A = draw(M, K, dist, 21)
+    B = draw(K, N, dist, 22)
+    ref = oracle.gemm(A, B)
+    for grouped, cross in ORDERS:
+        _, C = run(A, B, grouped=grouped, cross_tile=cross)
+        assert_within_bound(C, ref, A, B, f"{shape} {dist} grouped={grouped} cross={cross}")
+
+
+def test_orders_give_identical_results():
+    # tile order and cross-tile change only which CTA computes a tile and when;
+    # each tile's arithmetic is the same, so the outputs are bit-identical
+    A = draw(1000, 1200, "normal", 31)
+    B = draw(1200, 1500, "normal", 32)
+    outs = [run(A, B, grouped=g, cross_tile=c, G=G)[1]
+            for (g, c) in ORDERS for G in (1, 8)]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+# ------------------------------------------------------------------ predicated (non-TMA) paths
+
+@pytest.mark.parametrize("case", [
+    # name, M, N, K, A layout/pad/offset, B layout/pad/offset, C (ld, offset)
+    ("odd K rows", 300, 300, 257, ("row", 0, 0), ("row", 0, 0), None),
+    ("odd K col-major B", 260, 513, 257, ("row", 0, 0), ("col", 0, 0), None),
+    ("misaligned A base", 200, 300, 128, ("row", 0, 1), ("row", 0, 0), None),
+    ("misaligned B base", 200, 300, 128, ("row", 0, 0), ("col", 0, 3), None),
+    ("padded odd strides", 130, 270, 100, ("row", 3, 0), ("row", 5, 0), None),
+    ("odd C stride", 257, 300, 64, ("row", 0, 0), ("row", 0, 0), (301, 0)),
+    ("misaligned C base", 129, 256, 64, ("row", 0, 0), ("row", 0, 0), (256, 1)),
+    ("all predicated", 131, 259, 67, ("col", 1, 1), ("col", 3, 1), (263, 3)),
+])
+def test_predicated_paths_bit_exact(case):
+    name, M, N, K, la, lb, lc = case
+    A0 = draw(M, K, "int", 41)
+    B0 = draw(K, N, "int", 42)
+    ref = oracle.gemm(A0, B0)
+    A = relayout(A0, la[0], pad=la[1], offset=la[2])
+    B = relayout(B0, lb[0], pad=lb[1], offset=lb[2])
+    for grouped, cross in ORDERS:
+        Cd, C = run(A, B, grouped=grouped, cross_tile=cross, out_layout=lc)
+        assert np.array_equal(C, ref), f"{name} grouped={grouped} cross={cross}"
+        if lc is not None:
+            # nothing outside the logical C was written
+            ld, off = lc
+            buf = Cd.as_strided((Cd.untyped_storage().nbytes() // 4,), (1,), 0).cpu().numpy()
+            mask = np.ones(buf.size, bool)
+            for i in range(M):
+                mask[off + i * ld: off + i * ld + N] = False
+            assert np.isnan(buf[mask]).all(), name
+
+
+def test_predicated_random_within_bound():
+    A = relayout(draw(600, 257, "uniform", 51), "row")
+    B = relayout(draw(257, 700, "uniform", 52), "col")
+    ref = oracle.gemm(A, B)
+    _, C = run(A, B)
+    assert_within_bound(C, ref, A, B, "K=257 predicated")
+
+
+# ------------------------------------------------------------------ degenerate sizes
+
+def test_k_zero_sets_c_to_zero():
+    A = torch.zeros(100, 0, dtype=torch.float16, device="cuda")
+    B = torch.zeros(0, 300, dtype=torch.float16, device="cuda")
+    C = torch.full((100, 300), 7.0, device="cuda")
+    gemm(A, B, C)
+    torch.cuda.synchronize()
+    assert (C == 0).all()
+
+
+def test_empty_outputs_are_noops():
+    A = torch.ones(0, 64, dtype=torch.float16, device="cuda")
+    B = torch.ones(64, 30, dtype=torch.float16, device="cuda")
+    assert gemm(A, B).shape == (0, 30)
+    B = torch.ones(64, 0, dtype=torch.float16, device="cuda")
+    assert gemm(torch.ones(5, 64, dtype=torch.float16, device="cuda"), B).shape == (5, 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 4096, 64), (4096, 1, 64), (2, 3, 4),
+                                   (127, 255, 63), (128, 256, 64), (129, 257, 65)])
+def test_edge_shapes_bit_exact(M, N, K):
+    A = draw(M, K, "int", 61)
+    B = draw(K, N, "int", 62)
+    _, C = run(A, B)
+    assert np.array_equal(C, oracle.gemm(A, B))
+
+
+def test_overwrites_and_never_reads_c():
+    A = draw(256, 128, "int", 71)
+    B = draw(128, 512, "int", 72)
+    ref = oracle.gemm(A, B)
+    for fill in (float("nan"), float("inf"), 1e30):
+        Cd = torch.full((256, 512), fill, device="cuda")
+        gemm(to_dev(A), to_dev(B), Cd)
+        torch.cuda.synchronize()
+        assert np.array_equal(Cd.cpu().numpy().astype(np.float64), ref)
+
+
+def test_group_size_above_m_tiles_is_one_group():
+    A = draw(700, 300, "int", 81)
+    B = draw(300, 900, "int", 82)
+    ref = oracle.gemm(A, B)
+    for G in (5, 6, 1000, 2 ** 31 - 1):
+        assert np.array_equal(run(A, B, G=G)[1], ref)
+
+
+def test_invalid_arguments_raise():
+    A = torch.ones(8, 8, dtype=torch.float16, device="cuda")
+    with pytest.raises(GemmError):
+        gemm(A, A, group_size_m=0)
+    with pytest.raises(GemmError):
+        gemm(A, A, torch.empty(8, 16, device="cuda")[:, ::2])  # stride_cn = 2
+
+
+def test_kernel_resources():
+    info = kernel_info(0)
+    assert info["threads_per_cta"] == 192 and info["dynamic_smem"] <= 232448
+    assert info["regs_per_thread"] <= 255
+    cfg = get_config(16384, 16384)
+    assert cfg["grid"] == torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def test_repeated_calls_and_streams():
+    A = draw(512, 512, "int", 91)
+    B = draw(512, 512, "int", 92)
+    ref = oracle.gemm(A, B)
+    Ad, Bd = to_dev(A), to_dev(B)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(20):
+            outs.append(gemm(Ad, Bd))
+    s.synchronize()
+    for o in outs:
+        assert np.array_equal(o.cpu().numpy().astype(np.float64), ref)
+
+
+# ------------------------------------------------------------------ full workload sizes
+
+def _full(name, grouped=True, cross=True, exact_dist=False, count=64):
+    w = WORKLOADS[name]
+    A, B = w.operands()
+    if exact_dist:
+        A = draw(w.M, w.K, "int", w.seed)
+        B = draw(w.K, w.N, "int", w.seed + 1)
+        if w.b_layout != "row":
+            B = relayout(B, w.b_layout)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross)
+    check_sampled_tiles(C, A, B, count=count, seed=w.seed, exact=exact_dist, what=name)
+    check_row_col_sums(C, A, B, what=name)
+    return C
+
+
+@pytest.mark.parametrize("grouped", [True, False])
+def test_full_square_512(grouped):
+    w = WORKLOADS["square_512"]
+    A, B = w.operands()
+    _, C = run(A, B, grouped=grouped)
+    assert_within_bound(C, oracle.gemm(A, B), A, B, "512^3")
+
+
+@pytest.mark.parametrize("grouped", [True, False])
+def test_full_8192x8192x4096(grouped):
+    _full("square_8192x8192x4096", grouped=grouped)
+
+
+def test_full_16384x16384x4096_headline():
+    _full("square_16384x16384x4096", grouped=True, cross=True)
+
+
+def test_full_16384x16384x4096_row_major_no_cross():
+    _full("square_16384x16384x4096", grouped=False, cross=False, count=16)
+
+
+@pytest.mark.parametrize("K", [128, 512, 1024, 2048])
+@pytest.mark.parametrize("cross", [True, False])
+def test_full_k_sweep(K, cross):
+    _full(f"ksweep_16384x16384x{K}", grouped=True, cross=cross, count=32)
+
+
+def test_full_ragged_4000x5000x3000():
+    _full("ragged_4000x5000x3000")
+
+
+def test_full_ragged_8191x8191x257():
+    _full("ragged_8191x8191x257")
+
+
+def test_full_ragged_8191x8191x257_integer_exact():
+    _full("ragged_8191x8191x257", exact_dist=True, count=32)
