@@ -15,6 +15,7 @@ _LIB_NAME = "libgemm_f16.so"
 
 SCHED_GROUPED = 0x1
 SCHED_CROSS_TILE = 0x2
+SCHED_SINGLE_CTA = 0x4
 
 _STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
            3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT"}
@@ -51,7 +52,7 @@ def load_library():
     lib.gemm_f16.restype = ctypes.c_int
     lib.gemm_f16_tile_map.argtypes = [i32, i32, i32, u32, i32, vp, vp]
     lib.gemm_f16_tile_map.restype = ctypes.c_int
-    lib.gemm_f16_get_config.argtypes = [i64, i64, pi32, pi32, pi32, pi32, pi32]
+    lib.gemm_f16_get_config.argtypes = [i64, i64, u32, pi32, pi32, pi32, pi32, pi32]
     lib.gemm_f16_get_config.restype = ctypes.c_int
     lib.gemm_f16_kernel_info.argtypes = [i32, pi32, pi32, pi32, pi32]
     lib.gemm_f16_kernel_info.restype = ctypes.c_int
@@ -59,6 +60,8 @@ def load_library():
     lib.gemm_f16_sync_status.restype = ctypes.c_int
     lib.gemm_f16_set_wait_timeout.argtypes = [ctypes.c_uint64]
     lib.gemm_f16_set_wait_timeout.restype = ctypes.c_int
+    lib.gemm_f16_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.gemm_f16_selftest_wait_timeout.restype = ctypes.c_int
     lib.gemm_f16_status_str.argtypes = [ctypes.c_int]
     lib.gemm_f16_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -90,9 +93,14 @@ def gemm_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int,
                                    group_size_m, schedule_flags, stream)
 
 
+def sched_flags(grouped: bool = True, cross_tile: bool = True, single_cta: bool = False) -> int:
+    return ((SCHED_GROUPED if grouped else 0) | (SCHED_CROSS_TILE if cross_tile else 0)
+            | (SCHED_SINGLE_CTA if single_cta else 0))
+
+
 def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
          group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
-         stream=None) -> torch.Tensor:
+         single_cta: bool = False, stream=None) -> torch.Tensor:
     """C = A @ B with A [M,K], B [K,N] fp16 CUDA tensors; C fp32 [M,N].
 
     ``out`` (fp32, [M,N], unit column stride) is written if given, else
@@ -110,7 +118,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32 CUDA tensor of shape [M, N]")
-    flags = (SCHED_GROUPED if grouped else 0) | (SCHED_CROSS_TILE if cross_tile else 0)
+    flags = sched_flags(grouped, cross_tile, single_cta)
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
@@ -135,9 +143,10 @@ def tile_map(num_m_tiles: int, num_n_tiles: int, group_size_m: int, grouped: boo
     return out
 
 
-def get_config(M: int = 0, N: int = 0) -> dict:
+def get_config(M: int = 0, N: int = 0, single_cta: bool = False) -> dict:
     v = [ctypes.c_int32() for _ in range(5)]
-    _check(load_library().gemm_f16_get_config(M, N, *[ctypes.byref(x) for x in v]),
+    flags = sched_flags(single_cta=single_cta)
+    _check(load_library().gemm_f16_get_config(M, N, flags, *[ctypes.byref(x) for x in v]),
            "gemm_f16_get_config")
     return dict(zip(("bm", "bn", "bk", "stages", "grid"), (x.value for x in v)))
 
@@ -155,13 +164,19 @@ def sync_status(stream=None) -> int:
     return int(load_library().gemm_f16_sync_status(_stream_handle(stream)))
 
 
+def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None):
+    """Enqueue the bounded-wait self-test kernel (see the header)."""
+    _check(load_library().gemm_f16_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)),
+           "gemm_f16_selftest_wait_timeout")
+
+
 def set_wait_timeout(ns: int):
     _check(load_library().gemm_f16_set_wait_timeout(int(ns)), "gemm_f16_set_wait_timeout")
 
 
 def gemm_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Tensor = None, *,
                    workspace=None, group_size_m: int = 8, grouped: bool = True,
-                   cross_tile: bool = True, stream=None) -> torch.Tensor:
+                   cross_tile: bool = True, single_cta: bool = False, stream=None) -> torch.Tensor:
     """End-to-end call on HOST operands: copy A and B (pinned host fp16) to the
     device, run gemm_f16, copy C back into ``C_host`` (pinned fp32).
 
@@ -183,6 +198,6 @@ def gemm_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Ten
         A_dev.copy_(A_host, non_blocking=True)
         B_dev.copy_(B_host, non_blocking=True)
         gemm(A_dev, B_dev, C_dev, group_size_m=group_size_m, grouped=grouped,
-             cross_tile=cross_tile, stream=s)
+             cross_tile=cross_tile, single_cta=single_cta, stream=s)
         C_host.copy_(C_dev, non_blocking=True)
     return C_host

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libgemm_f16.so")
 SOURCES = [os.path.join(CSRC, "gemm_f16.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "ptx.cuh")] + \
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "gemm_pair.cuh", "ptx.cuh")] + \
     [os.path.join(INCLUDE, "gemm_f16.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

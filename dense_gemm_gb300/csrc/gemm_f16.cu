@@ -12,6 +12,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
+#include "gemm_pair.cuh"
 
 namespace {
 
@@ -27,6 +28,7 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_err = cudaSuccess;
     int num_sms = 0;
+    int max_pairs = 0;  // co-resident 2-CTA clusters of the pair kernel
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -51,6 +53,33 @@ cudaError_t set_smem_attr() {
                                 SMEM_BYTES);
 }
 
+template <bool S>
+cudaError_t set_pair_smem_attr() {
+    return cudaFuncSetAttribute(gemm_f16_pair<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                pair::SMEM_BYTES);
+}
+
+// How many 2-CTA clusters of the pair kernel fit on the device at once.
+int query_max_pairs(int num_sms) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(pair::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_pair<true>, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = num_sms / 2;
+    }
+    return n;
+}
+
 cudaError_t device_init(int dev, DeviceState **out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     DeviceState &d = g_dev[dev];
@@ -60,6 +89,9 @@ cudaError_t device_init(int dev, DeviceState **out) {
         if (e == cudaSuccess) e = set_smem_attr<true, false>();
         if (e == cudaSuccess) e = set_smem_attr<false, true>();
         if (e == cudaSuccess) e = set_smem_attr<false, false>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<true>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<false>();
+        if (e == cudaSuccess) d.max_pairs = query_max_pairs(d.num_sms);
         d.init_err = e;
     });
     *out = &d;
@@ -108,6 +140,20 @@ cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap
                    int grid, cudaStream_t stream) {
     gemm_f16_persistent<L, S><<<grid, cta_threads(L), SMEM_BYTES, stream>>>(a, b, c, p);
     return cudaGetLastError();
+}
+
+template <bool S>
+cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
+                        const Params &p, int grid, cudaStream_t stream) {
+    gemm_f16_pair<S><<<grid, pair::THREADS, pair::SMEM_BYTES, stream>>>(a, b, c, p);
+    return cudaGetLastError();
+}
+
+// Tile shape of the kernel that `flags` selects for TMA-loadable operands.
+void tile_shape(uint32_t flags, int *bm, int *bn) {
+    const bool single = (flags & GEMM_SCHED_SINGLE_CTA) != 0;
+    *bm = single ? BM : pair::TILE_M;
+    *bn = single ? BN : pair::TILE_N;
 }
 
 uint32_t next_epoch() {
@@ -174,24 +220,31 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    const int64_t nm = cdiv(M, BM), nn = cdiv(N, BN);
-    if (nm * nn > kMaxDim) return GEMM_ERR_UNSUPPORTED;
-
     // ---- path selection per tensor
     const bool a_tma = a_k ? tma_ok(A, K, stride_am, 2) : tma_ok(A, M, stride_ak, 2);
     const bool b_tma = b_n ? tma_ok(B, N, stride_bk, 2) : tma_ok(B, K, stride_bn, 2);
     const bool load_tma = a_tma && b_tma;
     const bool store_tma = tma_ok(C, N, stride_cm, 4);
+    // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
+    const bool use_pair = load_tma && !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
+    const int tile_m = use_pair ? pair::TILE_M : BM;
+    const int tile_n = use_pair ? pair::TILE_N : BN;
+    const int cta_m = use_pair ? pair::CTA_M : BM;    // A rows one CTA loads
+    const int cta_n = use_pair ? pair::CTA_N : BN;    // B columns one CTA loads
+    const int64_t nm = cdiv(M, tile_m), nn = cdiv(N, tile_n);
+    if (nm * nn > kMaxDim) return GEMM_ERR_UNSUPPORTED;
 
     CUtensorMap tmA, tmB, tmC;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
     std::memset(&tmC, 0, sizeof(tmC));
     if (load_tma) {
-        const bool okA = a_k ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, stride_am * 2, BK, BM)
+        const bool okA = a_k ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, stride_am * 2, BK,
+                                         cta_m)
                              : encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, M, K, stride_ak * 2,
                                          MN_CHUNK, BK);
-        const bool okB = b_k ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, stride_bn * 2, BK, BN)
+        const bool okB = b_k ? encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, K, N, stride_bn * 2, BK,
+                                         cta_n)
                              : encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, stride_bk * 2,
                                          MN_CHUNK, BK);
         if (!okA || !okB) return GEMM_ERR_CUDA;
@@ -222,23 +275,28 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
     p.num_kb = int32_t(cdiv(K, BK));
     p.a_mn = a_k ? 0u : 1u;
     p.b_mn = b_n ? 1u : 0u;
-    p.idesc = make_idesc(p.a_mn, p.b_mn);
+    p.idesc = make_idesc(p.a_mn, p.b_mn, use_pair ? 2 * pair::CTA_M : BM, tile_n);
     p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
     p.wait.timeout_ns = g_timeout_ns.load();
     p.wait.epoch = next_epoch();
 
-    const int grid = int(p.num_tiles < ds->num_sms ? p.num_tiles : ds->num_sms);
+    const int programs = use_pair ? ds->max_pairs : ds->num_sms;
+    const int grid_programs = int(p.num_tiles < programs ? p.num_tiles : programs);
+    const int grid = use_pair ? 2 * grid_programs : grid_programs;
     if (log_enabled())
         std::fprintf(stderr,
-                     "[gemm_f16] M=%lld N=%lld K=%lld tiles=%d grid=%d load=%s store=%s A=%s B=%s "
-                     "order=%s G=%d cross_tile=%u\n",
-                     (long long)M, (long long)N, (long long)K, p.num_tiles, grid,
+                     "[gemm_f16] M=%lld N=%lld K=%lld kernel=%s tiles=%d grid=%d load=%s store=%s A=%s "
+                     "B=%s order=%s G=%d cross_tile=%u\n",
+                     (long long)M, (long long)N, (long long)K, use_pair ? "cta-pair 256x256" : "one-cta 128x256",
+                     p.num_tiles, grid,
                      load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
                      p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
                      grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile);
 
     cudaError_t e;
-    if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, grid, stream);
+    if (use_pair) e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
+                                : launch_pair<false>(tmA, tmB, tmC, p, grid, stream);
+    else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, grid, stream);
     else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, grid, stream);
     else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, grid, stream);
     else e = launch<false, false>(tmA, tmB, tmC, p, grid, stream);
@@ -263,13 +321,17 @@ gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles, int32_
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn, int32_t *bk,
-                                  int32_t *stages, int32_t *grid) {
+gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t *bm, int32_t *bn,
+                                  int32_t *bk, int32_t *stages, int32_t *grid) {
     if (M < 0 || N < 0 || M > kMaxDim || N > kMaxDim) return GEMM_ERR_INVALID_ARG;
-    if (bm) *bm = BM;
-    if (bn) *bn = BN;
+    if (flags & ~GEMM_SCHED_ALL_FLAGS) return GEMM_ERR_INVALID_ARG;
+    const bool single = (flags & GEMM_SCHED_SINGLE_CTA) != 0;
+    int tm, tn;
+    tile_shape(flags, &tm, &tn);
+    if (bm) *bm = tm;
+    if (bn) *bn = tn;
     if (bk) *bk = BK;
-    if (stages) *stages = STAGES;
+    if (stages) *stages = single ? STAGES : pair::STAGES;
     if (grid) {
         *grid = 0;
         if (M > 0 && N > 0) {
@@ -277,8 +339,9 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn
             DeviceState *ds = nullptr;
             if (cudaGetDevice(&dev) != cudaSuccess || device_init(dev, &ds) != cudaSuccess)
                 return GEMM_ERR_CUDA;
-            const int64_t tiles = cdiv(M, BM) * cdiv(N, BN);
-            *grid = int32_t(tiles < ds->num_sms ? tiles : ds->num_sms);
+            const int64_t tiles = cdiv(M, tm) * cdiv(N, tn);
+            const int64_t programs = single ? ds->num_sms : ds->max_pairs;
+            *grid = int32_t(tiles < programs ? tiles : programs);
         }
     }
     return GEMM_OK;
@@ -286,7 +349,7 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn
 
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
                                    int32_t *dynamic_smem, int32_t *threads) {
-    if (variant < 0 || variant > 3) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 5) return GEMM_ERR_INVALID_ARG;
     cudaFuncAttributes a;
     cudaError_t e;
     int thr;
@@ -294,14 +357,25 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *stat
         case 0: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, true>); thr = cta_threads(true); break;
         case 1: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, false>); thr = cta_threads(true); break;
         case 2: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, true>); thr = cta_threads(false); break;
-        default: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, false>); thr = cta_threads(false); break;
+        case 3: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, false>); thr = cta_threads(false); break;
+        case 4: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true>); thr = pair::THREADS; break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false>); thr = pair::THREADS; break;
     }
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;
     if (static_smem) *static_smem = int32_t(a.sharedSizeBytes);
-    if (dynamic_smem) *dynamic_smem = SMEM_BYTES;
+    if (dynamic_smem) *dynamic_smem = variant >= 4 ? pair::SMEM_BYTES : SMEM_BYTES;
     if (threads) *threads = thr;
     return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t stream_) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000ull) return GEMM_ERR_INVALID_ARG;
+    WaitCtl w;
+    w.timeout_ns = timeout_ns;
+    w.epoch = next_epoch();
+    wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(w);
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_f16_sync_status(gemm_stream_t stream_) {

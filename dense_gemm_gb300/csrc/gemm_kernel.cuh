@@ -88,11 +88,13 @@ __device__ __forceinline__ bool launch_aborted(uint32_t epoch) {
 }
 
 // Slow path of a bounded wait. `bail` = also stop when another CTA of this
-// launch gave up. Returns false when the wait did not complete.
+// launch gave up. kCluster: acquire at cluster scope (the barrier receives
+// arrivals from the peer CTA). Returns false when the wait did not complete.
+template <bool kCluster = false>
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl w, bool bail) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((n & 15u) == 0) {
             if (bail && launch_aborted(w.epoch)) return false;
             if (global_timer_ns() - t0 > w.timeout_ns) {
@@ -104,9 +106,24 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitC
     }
 }
 
+// Waits made while cleaning up after an abort (copies or MMAs still in flight)
+// use at least this bound, so that a very short user timeout cannot free TMEM
+// or shared memory that asynchronous work is still using.
+constexpr uint64_t kCleanupFloorNs = 100000000ull;  // 100 ms
+
+__device__ __forceinline__ WaitCtl cleanup_wait(WaitCtl w) {
+    if (w.timeout_ns < kCleanupFloorNs) w.timeout_ns = kCleanupFloorNs;
+    return w;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtl w) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, w, true);
+    return mbar_wait_slow<false>(bar, parity, w, true);
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, WaitCtl w) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    return mbar_wait_slow<true>(bar, parity, w, true);
 }
 
 // ------------------------------------------------------------------ scheduler
@@ -158,13 +175,14 @@ struct Params {
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32, A/B fp16, dense,
-// M = 128, N = 256, per-operand major-ness.
-__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_mn, uint32_t b_mn) {
+// per-operand major-ness, MMA shape M x N (M = 128 for one CTA, 256 for a pair).
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t a_mn, uint32_t b_mn, uint32_t m,
+                                                  uint32_t n) {
     return (1u << 4)                 // D format: f32
            | (0u << 7) | (0u << 10)  // A, B format: f16
            | (a_mn << 15) | (b_mn << 16)
-           | (uint32_t(BN >> 3) << 17)   // N / 8
-           | (uint32_t(BM >> 4) << 24);  // M / 16
+           | ((n >> 3) << 17)   // N / 8
+           | ((m >> 4) << 24);  // M / 16
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 family layout):
@@ -224,6 +242,56 @@ __device__ __forceinline__ void load_operand_tile(uint32_t dst, const uint16_t *
             w[e >> 1] = lo | (hi << 16);
         }
         st_shared_v4(dst + off, w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ------------------------------------------------------------------ epilogue
+// Drains one accumulator of this CTA to C: the calling warp reads TMEM lanes
+// t_row.lane .. +31 (tile rows row0 .. row0+31) across BN columns in chunks of
+// 32, and writes C[row0 + r][col_base + c] for rows < M and columns < N.
+// TMA store: 128-byte-swizzled staging (two buffers per warp) + bulk tensor
+// store, which clips the M/N edges. Otherwise: transpose through the staging
+// buffer so each store instruction writes 32 consecutive floats of one row.
+// `drained()` runs on every lane right after the last TMEM load of the tile.
+template <bool kTmaStore, typename Drained>
+__device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int64_t col_base,
+                                              const Params &p, const CUtensorMap *tmC, uint32_t stg,
+                                              uint32_t &buf, int lane, Drained drained) {
+#pragma unroll 1
+    for (int c = 0; c < BN / EPI_COLS; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_row + c * EPI_COLS, v);
+        tmem_ld_wait();
+        if (c == BN / EPI_COLS - 1) drained();
+        const int64_t col0 = col_base + c * EPI_COLS;
+        if (kTmaStore) {
+            const uint32_t dst = stg + buf * EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();  // buffer free again
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(dst + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, dst, int32_t(col0), int32_t(row0));
+                bulk_commit_group();
+            }
+            buf ^= 1u;
+        } else {
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            __syncwarp();
+            const int64_t col = col0 + lane;
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+                const uint32_t bits = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+                const int64_t row = row0 + r;
+                if (row < p.M && col < p.N) p.C[row * p.scm + col] = __uint_as_float(bits);
+            }
+        }
     }
 }
 
@@ -329,7 +397,8 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                     // Let the copies this thread started land before the CTA exits.
                     const uint32_t n = issued < STAGES ? issued : STAGES;
                     for (uint32_t q = issued - n; q < issued; ++q)
-                        mbar_wait_slow(full_bar(q % STAGES), (q / STAGES) & 1u, p.wait, false);
+                        mbar_wait_slow(full_bar(q % STAGES), (q / STAGES) & 1u, cleanup_wait(p.wait),
+                                       false);
                 }
             }
             __syncwarp();
@@ -390,7 +459,7 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
             }
             // No MMA may still be writing TMEM when it is freed.
             mma_commit(drain_bar);
-            mbar_wait_slow(drain_bar, 0, p.wait, false);
+            mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false);
         }
         __syncwarp();
     } else {
@@ -410,52 +479,11 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
             if (!ready) break;
             tc_fence_after();
             const int64_t row0 = int64_t(tm) * BM + q * 32;
-            const int64_t col_base = int64_t(tn) * BN;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN / EPI_COLS; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + c * EPI_COLS, v);
-                tmem_ld_wait();
-                if (c == BN / EPI_COLS - 1) {
-                    tc_fence_before();
-                    mbar_arrive(tempty_bar(acc));  // accumulator may be overwritten
-                }
-                const int64_t col0 = col_base + c * EPI_COLS;
-                if (kTmaStore) {
-                    const uint32_t dst = stg + buf * EPI_BUF_BYTES;
-                    if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();  // buffer free again
-                    __syncwarp();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        st_shared_v4(dst + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2],
-                                     v[4 * u + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (row0 < p.M && col0 < p.N)
-                            tma_store_2d(&tmC, dst, int32_t(col0), int32_t(row0));
-                        bulk_commit_group();
-                    }
-                    buf ^= 1u;
-                } else {
-                    // transpose through shared memory so each store instruction
-                    // writes 32 consecutive floats of one row
-                    __syncwarp();
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2],
-                                     v[4 * u + 3]);
-                    __syncwarp();
-                    const int64_t col = col0 + lane;
-#pragma unroll 4
-                    for (int r = 0; r < 32; ++r) {
-                        const uint32_t bits = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
-                        const int64_t row = row0 + r;
-                        if (row < p.M && col < p.N) p.C[row * p.scm + col] = __uint_as_float(bits);
-                    }
-                }
-            }
+            epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane, [&] {
+                tc_fence_before();
+                mbar_arrive(tempty_bar(acc));  // accumulator may be overwritten
+            });
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -471,6 +499,19 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
 }
 
 // ------------------------------------------------------------------ helpers
+// Failure-detection self-test: one thread waits, through the same bounded wait
+// the GEMM roles use, on an mbarrier that nothing ever arrives on. The wait runs
+// out after `timeout_ns`, records GEMM_ERR_TIMEOUT in the sticky status and
+// returns; the context stays usable.
+__global__ void wait_timeout_selftest_kernel(WaitCtl w) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_addr(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait(b, 0, w);  // phase 0 never completes
+}
+
 __global__ void tile_map_kernel(Sched s, int32_t num_tiles, int32_t *out) {
     if (threadIdx.x != 0) return;
     for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {

@@ -58,7 +58,9 @@ typedef enum {
 #define GEMM_SCHED_GROUPED 0x1u    /* grouped ("CTA swizzle") tile order; else row-major */
 #define GEMM_SCHED_CROSS_TILE 0x2u /* overlap the next tile's loads/MMAs with the current
                                       tile's epilogue; else drain at every tile boundary */
-#define GEMM_SCHED_ALL_FLAGS 0x3u
+#define GEMM_SCHED_SINGLE_CTA 0x4u /* one CTA per 128x256 tile instead of a CTA pair per
+                                      256x256 tile (same results, lower throughput) */
+#define GEMM_SCHED_ALL_FLAGS 0x7u
 
 /*
  * gemm_f16 — C = A @ B.
@@ -79,7 +81,11 @@ typedef enum {
  * Operands whose base address is 16-byte aligned and whose non-unit stride is
  * a multiple of 8 elements (A, B) or 4 elements (C) go through TMA; others
  * (e.g. K = 257 row-major) through a predicated load/store path with the same
- * results.
+ * results. With TMA-loadable A and B the work is split into 256x256 output
+ * tiles, each computed by a pair of CTAs on the two SMs of a TPC (tcgen05
+ * cta_group::2); otherwise, or with GEMM_SCHED_SINGLE_CTA, into 128x256 tiles
+ * of one CTA each. The tile order (row-major / grouped) applies to whichever
+ * tiles are used; a "program" of the persistent order is a CTA pair or a CTA.
  * Sizes: M, N, K >= 0, each < 2^31. M == 0 or N == 0: nothing is done.
  * K == 0: C is set to 0.
  * Returns GEMM_OK once the work is enqueued.
@@ -109,20 +115,23 @@ gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles,
                                 int32_t *out_dev, gemm_stream_t stream);
 
 /*
- * gemm_f16_get_config — tile shape and launch size of gemm_f16 for an M x N
- * output on the current device. Any output pointer may be NULL.
- * bm, bn, bk: CTA tile; stages: shared-memory ring depth; grid: persistent
- * CTAs = min(#SMs, cdiv(M,bm)*cdiv(N,bn)) (needs a device; set to 0 when
- * M or N is 0).
+ * gemm_f16_get_config — tile shape and launch size gemm_f16 uses for an M x N
+ * output with TMA-loadable operands and these schedule_flags, on the current
+ * device. Any output pointer may be NULL; unknown flag bits -> INVALID_ARG.
+ * bm, bn, bk: output tile (256x256 per CTA pair, or 128x256 per CTA with
+ * GEMM_SCHED_SINGLE_CTA) and K step; stages: shared-memory ring depth; grid:
+ * persistent programs (CTA pairs or CTAs) = min(co-resident programs,
+ * cdiv(M,bm)*cdiv(N,bn)) (needs a device; 0 when M or N is 0).
  */
-gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, int32_t *bm, int32_t *bn,
-                                  int32_t *bk, int32_t *stages, int32_t *grid);
+gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags, int32_t *bm,
+                                  int32_t *bn, int32_t *bk, int32_t *stages, int32_t *grid);
 
 /*
  * gemm_f16_kernel_info — compiled resource use of a kernel variant
- * (cudaFuncGetAttributes): variant 0 = TMA loads + TMA store, 1 = TMA loads +
- * predicated store, 2 = predicated loads + TMA store, 3 = predicated loads +
- * predicated store. Outputs may be NULL. Needs a device.
+ * (cudaFuncGetAttributes). One-CTA tiles: variant 0 = TMA loads + TMA store,
+ * 1 = TMA loads + predicated store, 2 = predicated loads + TMA store,
+ * 3 = predicated loads + predicated store. CTA-pair tiles: 4 = TMA store,
+ * 5 = predicated store. Outputs may be NULL. Needs a device.
  */
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *static_smem, int32_t *dynamic_smem,
@@ -142,6 +151,16 @@ gemm_status_t gemm_f16_sync_status(gemm_stream_t stream);
  * to launches enqueued after the call. ns must be >= 1000.
  */
 gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns);
+
+/*
+ * gemm_f16_selftest_wait_timeout — failure-detection self-test (the pages have
+ * no counterpart: they describe no failure handling). Enqueues one thread that
+ * waits, through the same bounded-wait routine as every wait inside gemm_f16,
+ * on an mbarrier nothing arrives on. After timeout_ns (1e3 .. 1e10) the wait
+ * gives up, the sticky status becomes GEMM_ERR_TIMEOUT (read and cleared by
+ * gemm_f16_sync_status) and the kernel returns; the CUDA context stays usable.
+ */
+gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t stream);
 
 /* gemm_f16_status_str — static, human-readable name of a status code. */
 const char *gemm_f16_status_str(gemm_status_t status);

@@ -29,6 +29,8 @@ def _gpu():
 
 
 ORDERS = [(True, True), (True, False), (False, True), (False, False)]  # (grouped, cross_tile)
+# (grouped, cross_tile, single_cta): CTA-pair 256x256 tiles and one-CTA 128x256 tiles
+VARIANTS = [(g, c, False) for (g, c) in ORDERS] + [(True, True, True), (False, False, True)]
 
 
 # ------------------------------------------------------------------ tile map
@@ -51,24 +53,25 @@ SMALL_SHAPES = [(1, 1, 1), (128, 256, 64), (129, 257, 65), (300, 600, 200), (64,
 
 
 @pytest.mark.parametrize("shape", SMALL_SHAPES)
-@pytest.mark.parametrize("grouped,cross", ORDERS)
-def test_integer_inputs_bit_exact(shape, grouped, cross):
+@pytest.mark.parametrize("grouped,cross,single", VARIANTS)
+def test_integer_inputs_bit_exact(shape, grouped, cross, single):
     M, N, K = shape
     A = draw(M, K, "int", 7 + M)
     B = draw(K, N, "int", 8 + N)
-    _, C = run(A, B, grouped=grouped, cross_tile=cross, G=3)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross, G=3, single_cta=single)
     assert np.array_equal(C, oracle.gemm(A, B))
 
 
 @pytest.mark.parametrize("a_layout,b_layout", [("row", "row"), ("row", "col"), ("col", "row"),
                                                ("col", "col")])
 @pytest.mark.parametrize("shape", [(200, 300, 136), (384, 512, 256), (130, 260, 72)])
-def test_operand_layouts_bit_exact(a_layout, b_layout, shape):
+@pytest.mark.parametrize("single", [False, True])
+def test_operand_layouts_bit_exact(a_layout, b_layout, shape, single):
     M, N, K = shape
     A = draw(M, K, "int", 11)
     B = draw(K, N, "int", 12)
     ref = oracle.gemm(A, B)
-    _, C = run(relayout(A, a_layout), relayout(B, b_layout))
+    _, C = run(relayout(A, a_layout), relayout(B, b_layout), single_cta=single)
     assert np.array_equal(C, ref)
 
 
@@ -82,9 +85,10 @@ def test_random_inputs_within_bound(shape, dist):
     A = draw(M, K, dist, 21)
     B = draw(K, N, dist, 22)
     ref = oracle.gemm(A, B)
-    for grouped, cross in ORDERS:
-        _, C = run(A, B, grouped=grouped, cross_tile=cross)
-        assert_within_bound(C, ref, A, B, f"{shape} {dist} grouped={grouped} cross={cross}")
+    for grouped, cross, single in VARIANTS:
+        _, C = run(A, B, grouped=grouped, cross_tile=cross, single_cta=single)
+        assert_within_bound(C, ref, A, B,
+                            f"{shape} {dist} grouped={grouped} cross={cross} single={single}")
 
 
 def test_orders_give_identical_results():
@@ -92,10 +96,11 @@ def test_orders_give_identical_results():
     # each tile's arithmetic is the same, so the outputs are bit-identical
     A = draw(1000, 1200, "normal", 31)
     B = draw(1200, 1500, "normal", 32)
-    outs = [run(A, B, grouped=g, cross_tile=c, G=G)[1]
-            for (g, c) in ORDERS for G in (1, 8)]
-    for o in outs[1:]:
-        assert np.array_equal(o, outs[0])
+    for single in (False, True):
+        outs = [run(A, B, grouped=g, cross_tile=c, G=G, single_cta=single)[1]
+                for (g, c) in ORDERS for G in (1, 8)]
+        for o in outs[1:]:
+            assert np.array_equal(o, outs[0])
 
 
 # ------------------------------------------------------------------ predicated (non-TMA) paths
@@ -110,6 +115,7 @@ def test_orders_give_identical_results():
     ("odd C stride", 257, 300, 64, ("row", 0, 0), ("row", 0, 0), (301, 0)),
     ("misaligned C base", 129, 256, 64, ("row", 0, 0), ("row", 0, 0), (256, 1)),
     ("all predicated", 131, 259, 67, ("col", 1, 1), ("col", 3, 1), (263, 3)),
+    ("pair tiles, predicated store", 300, 520, 128, ("row", 0, 0), ("col", 0, 0), (523, 1)),
 ])
 def test_predicated_paths_bit_exact(case):
     name, M, N, K, la, lb, lc = case
@@ -118,9 +124,9 @@ def test_predicated_paths_bit_exact(case):
     ref = oracle.gemm(A0, B0)
     A = relayout(A0, la[0], pad=la[1], offset=la[2])
     B = relayout(B0, lb[0], pad=lb[1], offset=lb[2])
-    for grouped, cross in ORDERS:
-        Cd, C = run(A, B, grouped=grouped, cross_tile=cross, out_layout=lc)
-        assert np.array_equal(C, ref), f"{name} grouped={grouped} cross={cross}"
+    for grouped, cross, single in VARIANTS:
+        Cd, C = run(A, B, grouped=grouped, cross_tile=cross, out_layout=lc, single_cta=single)
+        assert np.array_equal(C, ref), f"{name} grouped={grouped} cross={cross} single={single}"
         if lc is not None:
             # nothing outside the logical C was written
             ld, off = lc
@@ -159,11 +165,13 @@ def test_empty_outputs_are_noops():
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 4096, 64), (4096, 1, 64), (2, 3, 4),
-                                   (127, 255, 63), (128, 256, 64), (129, 257, 65)])
-def test_edge_shapes_bit_exact(M, N, K):
+                                   (127, 255, 63), (128, 256, 64), (129, 257, 65),
+                                   (255, 255, 8), (256, 256, 64), (257, 513, 72), (384, 128, 16)])
+@pytest.mark.parametrize("single", [False, True])
+def test_edge_shapes_bit_exact(M, N, K, single):
     A = draw(M, K, "int", 61)
     B = draw(K, N, "int", 62)
-    _, C = run(A, B)
+    _, C = run(A, B, single_cta=single)
     assert np.array_equal(C, oracle.gemm(A, B))
 
 
@@ -195,11 +203,15 @@ def test_invalid_arguments_raise():
 
 
 def test_kernel_resources():
-    info = kernel_info(0)
-    assert info["threads_per_cta"] == 192 and info["dynamic_smem"] <= 232448
-    assert info["regs_per_thread"] <= 255
-    cfg = get_config(16384, 16384)
-    assert cfg["grid"] == torch.cuda.get_device_properties(0).multi_processor_count
+    for v in range(6):
+        info = kernel_info(v)
+        assert info["dynamic_smem"] <= 232448 and info["regs_per_thread"] <= 255
+        assert info["threads_per_cta"] in (192, 288)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert get_config(16384, 16384, single_cta=True)["grid"] == sms
+    pairs = get_config(16384, 16384)["grid"]
+    assert sms // 2 - 8 <= pairs <= sms // 2
+    assert get_config(512, 512)["grid"] == 4
 
 
 def test_repeated_calls_and_streams():
@@ -219,7 +231,7 @@ def test_repeated_calls_and_streams():
 
 # ------------------------------------------------------------------ full workload sizes
 
-def _full(name, grouped=True, cross=True, exact_dist=False, count=64):
+def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=False):
     w = WORKLOADS[name]
     A, B = w.operands()
     if exact_dist:
@@ -227,7 +239,7 @@ def _full(name, grouped=True, cross=True, exact_dist=False, count=64):
         B = draw(w.K, w.N, "int", w.seed + 1)
         if w.b_layout != "row":
             B = relayout(B, w.b_layout)
-    _, C = run(A, B, grouped=grouped, cross_tile=cross)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross, single_cta=single)
     check_sampled_tiles(C, A, B, count=count, seed=w.seed, exact=exact_dist, what=name)
     check_row_col_sums(C, A, B, what=name)
     return C
@@ -254,6 +266,10 @@ def test_full_16384x16384x4096_row_major_no_cross():
     _full("square_16384x16384x4096", grouped=False, cross=False, count=16)
 
 
+def test_full_16384x16384x4096_single_cta():
+    _full("square_16384x16384x4096", grouped=True, cross=True, count=16, single=True)
+
+
 @pytest.mark.parametrize("K", [128, 512, 1024, 2048])
 @pytest.mark.parametrize("cross", [True, False])
 def test_full_k_sweep(K, cross):
@@ -270,3 +286,17 @@ def test_full_ragged_8191x8191x257():
 
 def test_full_ragged_8191x8191x257_integer_exact():
     _full("ragged_8191x8191x257", exact_dist=True, count=32)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_bounded_wait_times_out_and_context_survives():
+    from dense_gemm_gb300 import selftest_wait_timeout
+    assert sync_status() == 0
+    selftest_wait_timeout(2_000_000)  # 2 ms: an mbarrier nothing arrives on
+    assert sync_status() == 4          # GEMM_ERR_TIMEOUT, read and cleared
+    assert sync_status() == 0
+    # the next GEMM on the same context is correct
+    A = draw(300, 200, "int", 99)
+    B = draw(200, 400, "int", 98)
+    assert np.array_equal(run(A, B)[1], oracle.gemm(A, B))
