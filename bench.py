@@ -52,6 +52,11 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="approximate CPU time of the oracle sample")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--single-cta", action="store_true",
+                   help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
+    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas"],
+                   default=None,
+                   help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
 
 
@@ -159,6 +164,23 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", str(rank)))
     return rank, world, local
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest `value` across the ranks of the default process group
+    (timings: the job takes as long as its slowest rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_rank_step: float, steps: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's work divided by the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
 
 
 def l2_note(w):
@@ -272,7 +294,7 @@ def run_gpu(args, w):
 
     def step():
         gemm(A, B, C, group_size_m=args.group_size, grouped=grouped, cross_tile=cross,
-             stream=stream)
+             single_cta=args.single_cta, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -307,17 +329,13 @@ def run_gpu(args, w):
         dist.barrier()
     status = sync_status(stream)
     per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(K_steps)]
-    total_ms = ev[0].elapsed_time(ev[K_steps])
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[K_steps]), dev)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
     if sampler:
         sampler.stop()
 
     flops = 2.0 * w.M * w.N * w.K
-    value = world * flops * K_steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(world, flops, K_steps, total_ms)
     avg_launch_ms = statistics.mean(per_launch_ms)
     med_launch_ms = statistics.median(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
@@ -331,7 +349,7 @@ def run_gpu(args, w):
         ws = (torch.empty_strided(A.shape, A.stride(), dtype=A.dtype, device=dev),
               torch.empty_strided(B.shape, B.stride(), dtype=B.dtype, device=dev), C)
         gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
-                       grouped=grouped, cross_tile=cross, stream=stream)
+                       grouped=grouped, cross_tile=cross, single_cta=args.single_cta, stream=stream)
         torch.cuda.synchronize(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
@@ -339,16 +357,13 @@ def run_gpu(args, w):
         e0.record(stream)
         for _ in range(args.e2e_steps):
             gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
-                           grouped=grouped, cross_tile=cross, stream=stream)
+                           grouped=grouped, cross_tile=cross, single_cta=args.single_cta,
+                           stream=stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         in_bytes = A_host.untyped_storage().nbytes() + B_host.untyped_storage().nbytes()
-        e2e = {"value": world * flops * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_throughput(world, flops, args.e2e_steps, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * w.M * w.N,
                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
                "api": "dense_gemm_gb300.gemm_from_host (pinned host A, B, C)"}
@@ -366,7 +381,8 @@ def run_gpu(args, w):
     intensity = flops / compulsory
     bound_tflops = min(NVL72_SPEC_FP16_TFLOPS, hbm * 1e9 * intensity / 1e12)
     traffic = recorded_traffic(w.name, args.order, cross)
-    info = kernel_info(0)
+    info = kernel_info(0 if args.single_cta else 4)
+    sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
 
     line = {
         "metric": "FP16 GEMM TFLOPS (2MNK/s) and % of GB300 dense FP16 peak",
@@ -374,7 +390,9 @@ def run_gpu(args, w):
         "warmup": args.warmup, "ms_per_step": total_ms / K_steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": workload_config(w, args, {"parallelism": f"independent replicas x{world}",
-                                            "accumulate": "f32", "output": "f32"}),
+                                            "accumulate": "f32", "output": "f32",
+                                            "tiles": "one CTA, 128x256" if args.single_cta
+                                            else "CTA pair (cta_group::2), 256x256"}),
         "pct_of_peak": {"nvl72_spec_2500": 100.0 * value / world / NVL72_SPEC_FP16_TFLOPS,
                         "nominal_2250": 100.0 * value / world / NOMINAL_FP16_TFLOPS,
                         f"{peak_src}_bf16_{peak:g}": 100.0 * value / world / peak},
@@ -382,7 +400,10 @@ def run_gpu(args, w):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} cuBLAS bf16 burst (MEASURED_PEAKS.json) x nominal "
                                     "fp16/bf16 ratio 1.0",
-                     "kernel": "g16::gemm_f16_persistent<true,true>",
+                     "frac_of_sustained_peak": (achieved / sustained) if sustained else None,
+                     "sustained_peak": sustained,
+                     "kernel": ("g16::gemm_f16_persistent<true,true>" if args.single_cta
+                                else "g16::gemm_f16_pair<true>"),
                      "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": avg_launch_ms, "median_launch_ms": med_launch_ms,
                      "workload_roofline_tflops_min_P_BWxI": bound_tflops,
@@ -401,9 +422,75 @@ def run_gpu(args, w):
     return 0 if status == 0 else 1
 
 
+# ---------------------------------------------------------------- studies
+
+def run_sweep(args):
+    """Device-timed points of one study, one JSON line each:
+    order  - grouped vs row-major tile order (8192^2 and 16384^2, K = 4096);
+    ksweep - cross-tile on vs off, 16384^2, K in {128 ... 4096};
+    kernel - CTA-pair vs one-CTA tiles on the headline workload;
+    persistence - the pages' four variants (tiled / persistent x row-major /
+                  grouped) at 8192^2 and 16384^2, K = 4096;
+    cublas - context line: torch.matmul (cuBLAS, fp16 output) on 8192^2 and
+             16384^2, K = 4096, next to gemm_f16 on the same operands."""
+    import torch
+    from dense_gemm_gb300 import gemm, sync_status
+    from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
+
+    dev = torch.device("cuda", 0)
+    if args.sweep == "order":
+        names = ["square_8192x8192x4096", HEADLINE]
+        points = [dict(grouped=g, cross_tile=True, single_cta=False) for g in (True, False)]
+    elif args.sweep == "ksweep":
+        names = [n for n in WORKLOADS if n.startswith("ksweep_")]
+        points = [dict(grouped=True, cross_tile=c, single_cta=False) for c in (True, False)]
+    elif args.sweep == "cublas":
+        names = ["square_8192x8192x4096", HEADLINE]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False), "torch.matmul"]
+    elif args.sweep == "persistence":
+        names = ["square_8192x8192x4096", HEADLINE]
+        points = [dict(grouped=g, cross_tile=True, single_cta=False, persistent=per)
+                  for per in (False, True) for g in (False, True)]
+    else:
+        names = [HEADLINE]
+        points = [dict(grouped=True, cross_tile=True, single_cta=s) for s in (False, True)]
+    steps = max(args.steps, 1)
+    for name in names:
+        w = WORKLOADS[name]
+        A_host, B_host = w.operands()
+        A, B = A_host.to(dev), B_host.to(dev)
+        C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        for pt in points:
+            if pt == "torch.matmul":
+                run = lambda: torch.matmul(A, B)  # noqa: E731  (cuBLAS, fp16 output)
+                desc = {"impl": "torch.matmul (cuBLAS), fp16 output"}
+            else:
+                run = lambda: gemm(A, B, C, group_size_m=args.group_size, **pt)  # noqa: E731
+                desc = {"impl": "gemm_f16", **pt, "group_size_m": args.group_size}
+            for _ in range(max(args.warmup, 3)):
+                run()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                run()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / steps
+            flops = 2.0 * w.M * w.N * w.K
+            print(json.dumps({"study": args.sweep, "workload": name, "M": w.M, "N": w.N, "K": w.K,
+                              **desc, "steps": steps, "ms_per_launch": ms,
+                              "tflops": flops / (ms * 1e-3) / 1e12, "status": sync_status()}),
+                  flush=True)
+        del A, B, C
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
+    if args.sweep:
+        return run_sweep(args)
     w = WORKLOADS[args.workload or HEADLINE]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -277,21 +277,27 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
     p.b_mn = b_n ? 1u : 0u;
     p.idesc = make_idesc(p.a_mn, p.b_mn, use_pair ? 2 * pair::CTA_M : BM, tile_n);
     p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
+    // C is written once and never read again: its stores carry an evict-first
+    // L2 policy. Operand loads keep the default policy (an evict-last hint on
+    // them measured slower: tensor-pipe activity 86.3 % -> 83.7 % at 16384^2).
+    p.l2_mode = 1u;
     p.wait.timeout_ns = g_timeout_ns.load();
     p.wait.epoch = next_epoch();
 
-    const int programs = use_pair ? ds->max_pairs : ds->num_sms;
+    const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT);
+    const int programs = !persistent ? p.num_tiles : use_pair ? ds->max_pairs : ds->num_sms;
     const int grid_programs = int(p.num_tiles < programs ? p.num_tiles : programs);
+    if (use_pair && int64_t(grid_programs) * 2 > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     const int grid = use_pair ? 2 * grid_programs : grid_programs;
     if (log_enabled())
         std::fprintf(stderr,
                      "[gemm_f16] M=%lld N=%lld K=%lld kernel=%s tiles=%d grid=%d load=%s store=%s A=%s "
-                     "B=%s order=%s G=%d cross_tile=%u\n",
+                     "B=%s order=%s G=%d cross_tile=%u persistent=%d\n",
                      (long long)M, (long long)N, (long long)K, use_pair ? "cta-pair 256x256" : "one-cta 128x256",
                      p.num_tiles, grid,
                      load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
                      p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
-                     grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile);
+                     grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile, int(persistent));
 
     cudaError_t e;
     if (use_pair) e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
@@ -340,7 +346,8 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
             if (cudaGetDevice(&dev) != cudaSuccess || device_init(dev, &ds) != cudaSuccess)
                 return GEMM_ERR_CUDA;
             const int64_t tiles = cdiv(M, tm) * cdiv(N, tn);
-            const int64_t programs = single ? ds->num_sms : ds->max_pairs;
+            const int64_t programs = (flags & GEMM_SCHED_NON_PERSISTENT) ? tiles
+                                     : single ? ds->num_sms : ds->max_pairs;
             *grid = int32_t(tiles < programs ? tiles : programs);
         }
     }

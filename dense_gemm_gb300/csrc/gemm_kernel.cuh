@@ -90,14 +90,23 @@ __device__ __forceinline__ bool launch_aborted(uint32_t epoch) {
 // Slow path of a bounded wait. `bail` = also stop when another CTA of this
 // launch gave up. kCluster: acquire at cluster scope (the barrier receives
 // arrivals from the peer CTA). Returns false when the wait did not complete.
+// The loop polls the barrier tightly: the clock and the launch-wide abort flag
+// (a global-memory load) are consulted only every 1024 polls, so that a
+// completed phase is noticed within one poll; these waits sit on the
+// producer -> MMA -> producer hand-off that feeds the tensor pipe.
 template <bool kCluster = false>
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtl w, bool bail) {
-    const uint64_t t0 = global_timer_ns();
+    uint64_t t0 = 0;
     for (uint32_t n = 1;; ++n) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-        if ((n & 15u) == 0) {
+        if ((n & 1023u) == 0) {
+            const uint64_t t = global_timer_ns();
+            if (t0 == 0) {
+                t0 = t;
+                continue;
+            }
             if (bail && launch_aborted(w.epoch)) return false;
-            if (global_timer_ns() - t0 > w.timeout_ns) {
+            if (t - t0 > w.timeout_ns) {
                 atomicCAS(&g_status, 0u, kStatusTimeout);
                 atomicExch(&g_abort_epoch, w.epoch);
                 return false;
@@ -171,6 +180,7 @@ struct Params {
     uint32_t b_mn;      // 1: B is N-major
     uint32_t idesc;     // tcgen05 instruction descriptor
     uint32_t cross_tile;
+    uint32_t l2_mode;   // bit 0: C stores evict-first; bit 1: A/B loads evict-last (pair kernel)
     WaitCtl wait;
 };
 
@@ -200,6 +210,26 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 __device__ __forceinline__ uint64_t operand_desc(uint32_t tile_addr, uint32_t mn_major, int k16) {
     if (mn_major) return smem_desc(tile_addr + uint32_t(k16) * (UMMA_K * 128), MN_CHUNK_BYTES, 1024);
     return smem_desc(tile_addr + uint32_t(k16) * (UMMA_K * 2), 16, 1024);
+}
+
+// Descriptor stepping without rebuilding: the start address sits in the low
+// 14 bits in units of 16 bytes, and every shared-memory address here is below
+// 256 KiB, so adding (byte offset >> 4) to a descriptor moves its start address
+// without carrying into the other fields. The MMA-issuing thread is on the
+// critical path of the tensor pipe, so it only adds precomputed steps.
+struct DescStep {
+    uint64_t base;       // descriptor of stage 0, k16 slice 0
+    uint32_t stage;      // (stage bytes) >> 4
+    uint32_t k16;        // (bytes between consecutive k16 slices) >> 4
+};
+
+__device__ __forceinline__ DescStep make_desc_step(uint32_t tile_addr, uint32_t mn_major,
+                                                   uint32_t stage_bytes) {
+    DescStep d;
+    d.base = operand_desc(tile_addr, mn_major, 0);
+    d.stage = stage_bytes >> 4;
+    d.k16 = (mn_major ? UMMA_K * 128u : UMMA_K * 2u) >> 4;
+    return d;
 }
 
 // Byte offset of 16-byte unit `unit` (0..7) of 128-byte row `row` after the
@@ -274,7 +304,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                if (row0 < p.M && col0 < p.N) tma_store_2d(tmC, dst, int32_t(col0), int32_t(row0));
+                if (row0 < p.M && col0 < p.N) {
+                    if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
+                        tma_store_2d_hint(tmC, dst, int32_t(col0), int32_t(row0), l2_policy_evict_first());
+                    else
+                        tma_store_2d(tmC, dst, int32_t(col0), int32_t(row0));
+                }
                 bulk_commit_group();
             }
             buf ^= 1u;
@@ -431,37 +466,44 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
         }
     } else if (warp == MMA_WARP) {
         // ============================================================ MMA issuer
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            int32_t it = 0;
-            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += grid, ++it) {
-                const uint32_t acc = it & 1, use = it >> 1;
-                if (!mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.wait)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
-                for (int32_t kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, p.wait)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a_tile = sA + stage * A_STAGE_BYTES;
-                    const uint32_t b_tile = sB + stage * B_STAGE_BYTES;
-#pragma unroll
-                    for (int k16 = 0; k16 < BK / UMMA_K; ++k16) {
-                        mma_f16(d_tmem, operand_desc(a_tile, p.a_mn, k16),
-                                operand_desc(b_tile, p.b_mn, k16), p.idesc,
-                                (kb > 0 || k16 > 0) ? 1u : 0u);
-                    }
-                    mma_commit(empty_bar(stage));  // slot reusable once these MMAs finish
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-                }
-                if (!ok) break;
-                mma_commit(tfull_bar(acc));  // accumulator complete
+        // The whole warp runs this loop with warp-uniform values; every lane
+        // waits on the barriers (votes keep the outcome uniform) and one
+        // elected lane issues each MMA and commit.
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        int32_t it = 0;
+        const DescStep da = make_desc_step(sA, p.a_mn, A_STAGE_BYTES);
+        const DescStep db = make_desc_step(sB, p.b_mn, B_STAGE_BYTES);
+        const uint32_t idesc = p.idesc;
+        for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += grid, ++it) {
+            const uint32_t acc = it & 1, use = it >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.wait))) {
+                ok = false;
+                break;
             }
-            // No MMA may still be writing TMEM when it is freed.
-            mma_commit(drain_bar);
-            mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false);
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + acc * BN;
+            for (int32_t kb = 0; kb < num_kb; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.wait))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t a0 = da.base + stage * da.stage;
+                const uint64_t b0 = db.base + stage * db.stage;
+#pragma unroll
+                for (int k16 = 0; k16 < BK / UMMA_K; ++k16)
+                    mma_f16_elect(d_tmem, a0 + k16 * da.k16, b0 + k16 * db.k16, idesc,
+                                  (kb | k16) != 0 ? 1u : 0u);
+                mma_commit_elect(empty_bar(stage));  // slot reusable once these MMAs finish
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            mma_commit_elect(tfull_bar(acc));  // accumulator complete
         }
-        __syncwarp();
+        // No MMA may still be writing TMEM when it is freed.
+        mma_commit_elect(drain_bar);
+        __all_sync(0xffffffffu, mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false));
     } else {
         // ============================================================ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access = tile rows q*32..q*32+31

@@ -104,6 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     if (warp == 0) {
         // ============================================================ producer (both CTAs)
         if (lane == 0) {
+            const uint64_t pol_ld = l2_policy_evict_last();
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             int32_t it = 0;
@@ -123,19 +124,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                     const int32_t k0 = kb * BK;
                     const uint32_t a_dst = sA + stage * pair::A_STAGE_BYTES;
                     const uint32_t b_dst = sB + stage * pair::B_STAGE_BYTES;
-                    if (!p.a_mn) {
-                        tma_load_2d_pair(a_dst, &tmA, k0, m0, fb);
-                    } else {
+                    if (p.l2_mode & 2u) {  // operand tiles are re-read by other pairs: keep in L2
+                        if (!p.a_mn) {
+                            tma_load_2d_pair_hint(a_dst, &tmA, k0, m0, fb, pol_ld);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < pair::CTA_M / MN_CHUNK; ++c)
-                            tma_load_2d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK, k0, fb);
-                    }
-                    if (!p.b_mn) {
-                        tma_load_2d_pair(b_dst, &tmB, k0, n0, fb);
-                    } else {
+                            for (int c = 0; c < pair::CTA_M / MN_CHUNK; ++c)
+                                tma_load_2d_pair_hint(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK,
+                                                      k0, fb, pol_ld);
+                        }
+                        if (!p.b_mn) {
+                            tma_load_2d_pair_hint(b_dst, &tmB, k0, n0, fb, pol_ld);
+                        } else {
 #pragma unroll
-                        for (int c = 0; c < pair::CTA_N / MN_CHUNK; ++c)
-                            tma_load_2d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK, k0, fb);
+                            for (int c = 0; c < pair::CTA_N / MN_CHUNK; ++c)
+                                tma_load_2d_pair_hint(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK,
+                                                      k0, fb, pol_ld);
+                        }
+                    } else {
+                        if (!p.a_mn) {
+                            tma_load_2d_pair(a_dst, &tmA, k0, m0, fb);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < pair::CTA_M / MN_CHUNK; ++c)
+                                tma_load_2d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK, k0, fb);
+                        }
+                        if (!p.b_mn) {
+                            tma_load_2d_pair(b_dst, &tmB, k0, n0, fb);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < pair::CTA_N / MN_CHUNK; ++c)
+                                tma_load_2d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK, k0, fb);
+                        }
                     }
                     ++issued;
                     if (++stage == pair::STAGES) { stage = 0; phase ^= 1u; }
@@ -161,37 +181,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         __syncwarp();
     } else if (warp == MMA_WARP) {
         // ============================================================ MMA issuer (CTA 0)
-        if (rank == 0 && lane == 0) {
+        // Whole warp, warp-uniform values; one elected lane issues (see the
+        // single-CTA kernel).
+        if (rank == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             int32_t it = 0;
+            const DescStep da = make_desc_step(sA, p.a_mn, pair::A_STAGE_BYTES);
+            const DescStep db = make_desc_step(sB, p.b_mn, pair::B_STAGE_BYTES);
+            const uint32_t idesc = p.idesc;
             for (int32_t tile = pair_id; ok && tile < p.num_tiles; tile += num_pairs, ++it) {
                 const uint32_t acc = it & 1, use = it >> 1;
                 // both CTAs' epilogues have released this accumulator (remote arrivals)
-                if (!mbar_wait_cluster(tempty_bar(acc), (use & 1u) ^ 1u, p.wait)) { ok = false; break; }
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_cluster(tempty_bar(acc), (use & 1u) ^ 1u, p.wait))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * pair::TILE_N;
                 for (int32_t kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, p.wait)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t a_tile = sA + stage * pair::A_STAGE_BYTES;
-                    const uint32_t b_tile = sB + stage * pair::B_STAGE_BYTES;
-#pragma unroll
-                    for (int k16 = 0; k16 < BK / UMMA_K; ++k16) {
-                        mma_f16_pair(d_tmem, operand_desc(a_tile, p.a_mn, k16),
-                                     operand_desc(b_tile, p.b_mn, k16), p.idesc,
-                                     (kb > 0 || k16 > 0) ? 1u : 0u);
+                    if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.wait))) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit_pair_mc(empty_bar(stage), 0x3);  // both CTAs' slots reusable
+                    tc_fence_after();
+                    const uint64_t a0 = da.base + stage * da.stage;
+                    const uint64_t b0 = db.base + stage * db.stage;
+#pragma unroll
+                    for (int k16 = 0; k16 < BK / UMMA_K; ++k16)
+                        mma_f16_pair_elect(d_tmem, a0 + k16 * da.k16, b0 + k16 * db.k16, idesc,
+                                           (kb | k16) != 0 ? 1u : 0u);
+                    mma_commit_pair_mc_elect(empty_bar(stage), 0x3);  // both CTAs' slots reusable
                     if (++stage == pair::STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                mma_commit_pair_mc(tfull_bar(acc), 0x3);  // both halves of the tile complete
+                mma_commit_pair_mc_elect(tfull_bar(acc), 0x3);  // both halves of the tile complete
             }
-            mma_commit_pair(drain_bar);
-            mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false);
+            mma_commit_pair_elect(drain_bar);
+            __all_sync(0xffffffffu, mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false));
         }
-        __syncwarp();
     } else {
         // ============================================================ epilogue (both CTAs)
         const int q = warp & 3;

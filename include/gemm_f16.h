@@ -60,7 +60,10 @@ typedef enum {
                                       tile's epilogue; else drain at every tile boundary */
 #define GEMM_SCHED_SINGLE_CTA 0x4u /* one CTA per 128x256 tile instead of a CTA pair per
                                       256x256 tile (same results, lower throughput) */
-#define GEMM_SCHED_ALL_FLAGS 0x7u
+#define GEMM_SCHED_NON_PERSISTENT 0x8u /* one program per tile (grid = #tiles, the hardware
+                                          assigns programs to SMs) instead of a persistent
+                                          grid of co-resident programs */
+#define GEMM_SCHED_ALL_FLAGS 0xFu
 
 /*
  * gemm_f16 — C = A @ B.
@@ -86,6 +89,9 @@ typedef enum {
  * cta_group::2); otherwise, or with GEMM_SCHED_SINGLE_CTA, into 128x256 tiles
  * of one CTA each. The tile order (row-major / grouped) applies to whichever
  * tiles are used; a "program" of the persistent order is a CTA pair or a CTA.
+ * GEMM_SCHED_NON_PERSISTENT launches one program per tile ([persistent]
+ * "naive tiled matmul" grid); program p then computes tile_id p only, and
+ * GEMM_SCHED_CROSS_TILE has nothing to overlap.
  * Sizes: M, N, K >= 0, each < 2^31. M == 0 or N == 0: nothing is done.
  * K == 0: C is set to 0.
  * Returns GEMM_OK once the work is enqueued.
@@ -121,7 +127,8 @@ gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles,
  * bm, bn, bk: output tile (256x256 per CTA pair, or 128x256 per CTA with
  * GEMM_SCHED_SINGLE_CTA) and K step; stages: shared-memory ring depth; grid:
  * persistent programs (CTA pairs or CTAs) = min(co-resident programs,
- * cdiv(M,bm)*cdiv(N,bn)) (needs a device; 0 when M or N is 0).
+ * cdiv(M,bm)*cdiv(N,bn)), or the tile count with GEMM_SCHED_NON_PERSISTENT
+ * (needs a device; 0 when M or N is 0).
  */
 gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags, int32_t *bm,
                                   int32_t *bn, int32_t *bk, int32_t *stages, int32_t *grid);

@@ -103,6 +103,19 @@ def test_orders_give_identical_results():
             assert np.array_equal(o, outs[0])
 
 
+@pytest.mark.parametrize("single", [False, True])
+@pytest.mark.parametrize("grouped", [False, True])
+@pytest.mark.parametrize("shape", [(640, 640, 640), (1000, 1200, 300), (129, 257, 65)])
+def test_non_persistent_grid_bit_exact(shape, grouped, single):
+    M, N, K = shape
+    A = draw(M, K, "int", 33)
+    B = draw(K, N, "int", 34)
+    _, C = run(A, B, grouped=grouped, single_cta=single, persistent=False, G=3)
+    assert np.array_equal(C, oracle.gemm(A, B))
+    cfg = get_config(M, N, single_cta=single, persistent=False)
+    assert cfg["grid"] == -(-M // cfg["bm"]) * -(-N // cfg["bn"])
+
+
 # ------------------------------------------------------------------ predicated (non-TMA) paths
 
 @pytest.mark.parametrize("case", [
