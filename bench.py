@@ -74,8 +74,8 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for rel in ("dense_gemm_gb300/csrc/gemm_kernel.cuh", "dense_gemm_gb300/csrc/ptx.cuh",
-                "dense_gemm_gb300/csrc/gemm_f16.cu"):
+    for rel in ("dense_gemm_gb300/csrc/gemm_kernel.cuh", "dense_gemm_gb300/csrc/gemm_pair.cuh",
+                "dense_gemm_gb300/csrc/ptx.cuh", "dense_gemm_gb300/csrc/gemm_f16.cu"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
