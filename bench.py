@@ -9,7 +9,7 @@ workload; the default workload is M = N = 16384, K = 4096, A and B row-major
 fp16 N(0,1), fp32 accumulate and output, grouped order with GROUP_SIZE_M = 8,
 cross-tile pipelining on. ``value`` is the device-timed throughput (CUDA
 events on the launching stream, inputs resident in HBM); ``e2e`` is the same
-metric through ``gemm_from_host`` with pinned host operands, host<->device
+metric through ``HostPipeline`` with pinned host operands, host<->device
 copies inside the timed region. Under torchrun every rank runs its own copy
 of the workload on its own GPU (independent problems, weak scaling).
 
@@ -54,7 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
-    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas"],
+    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
@@ -276,7 +276,7 @@ def run_gpu(args, w):
     import torch
     import torch.distributed as dist
 
-    from dense_gemm_gb300 import gemm, gemm_from_host, kernel_info, sync_status
+    from dense_gemm_gb300 import HostPipeline, gemm, kernel_info, sync_status
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -346,28 +346,30 @@ def run_gpu(args, w):
         A_pin = A_host.pin_memory()
         B_pin = B_host.pin_memory()
         C_pin = torch.empty((w.M, w.N), dtype=torch.float32, pin_memory=True)
-        ws = (torch.empty_strided(A.shape, A.stride(), dtype=A.dtype, device=dev),
-              torch.empty_strided(B.shape, B.stride(), dtype=B.dtype, device=dev), C)
-        gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
-                       grouped=grouped, cross_tile=cross, single_cta=args.single_cta, stream=stream)
-        torch.cuda.synchronize(dev)
+        del C  # the pipeline holds its own device buffers
+        torch.cuda.empty_cache()
+        pipe = HostPipeline(A, B, depth=2, group_size_m=args.group_size, grouped=grouped,
+                            cross_tile=cross, single_cta=args.single_cta, device=dev)
+        del A, B
+        for _ in range(2):  # warm-up: both buffer sets
+            pipe.submit(A_pin, B_pin, C_pin)
+        pipe.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
-        e0.record(stream)
+        e0.record(pipe.s_in)
         for _ in range(args.e2e_steps):
-            gemm_from_host(A_pin, B_pin, C_pin, workspace=ws, group_size_m=args.group_size,
-                           grouped=grouped, cross_tile=cross, single_cta=args.single_cta,
-                           stream=stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+            pipe.submit(A_pin, B_pin, C_pin)
+        e1.record(pipe.s_out)
+        pipe.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         in_bytes = A_host.untyped_storage().nbytes() + B_host.untyped_storage().nbytes()
         e2e = {"value": job_throughput(world, flops, args.e2e_steps, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * w.M * w.N,
                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
-               "api": "dense_gemm_gb300.gemm_from_host (pinned host A, B, C)"}
-        del A_pin, B_pin, C_pin
+               "api": "dense_gemm_gb300.HostPipeline (pinned host A, B -> device, gemm_f16, "
+                      "C -> pinned host; upload+GEMM of step i+1 overlap the download of step i)"}
+        del pipe, A_pin, B_pin, C_pin
 
     if rank != 0:
         if world > 1:
@@ -432,9 +434,11 @@ def run_sweep(args):
     persistence - the pages' four variants (tiled / persistent x row-major /
                   grouped) at 8192^2 and 16384^2, K = 4096;
     cublas - context line: torch.matmul (cuBLAS, fp16 output) on 8192^2 and
-             16384^2, K = 4096, next to gemm_f16 on the same operands."""
+             16384^2, K = 4096, next to gemm_f16 on the same operands;
+    splitk - gemm_f16 vs gemm_f16_splitk (automatic slices) on 512^3 and
+             1024^2 x 32768 (fewer tiles than CTA pairs)."""
     import torch
-    from dense_gemm_gb300 import gemm, sync_status
+    from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
 
     dev = torch.device("cuda", 0)
@@ -444,6 +448,9 @@ def run_sweep(args):
     elif args.sweep == "ksweep":
         names = [n for n in WORKLOADS if n.startswith("ksweep_")]
         points = [dict(grouped=True, cross_tile=c, single_cta=False) for c in (True, False)]
+    elif args.sweep == "splitk":
+        names = ["square_512", "longk_1024x1024x32768"]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False), "splitk"]
     elif args.sweep == "cublas":
         names = ["square_8192x8192x4096", HEADLINE]
         points = [dict(grouped=True, cross_tile=True, single_cta=False), "torch.matmul"]
@@ -464,6 +471,12 @@ def run_sweep(args):
             if pt == "torch.matmul":
                 run = lambda: torch.matmul(A, B)  # noqa: E731  (cuBLAS, fp16 output)
                 desc = {"impl": "torch.matmul (cuBLAS), fp16 output"}
+            elif pt == "splitk":
+                need, used = splitk_workspace_size(w.M, w.N, w.K, 0)
+                ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+                run = lambda: gemm_splitk(A, B, C, splits=0, workspace=ws,  # noqa: E731
+                                          group_size_m=args.group_size)
+                desc = {"impl": "gemm_f16_splitk", "splits": used, "workspace_bytes": need}
             else:
                 run = lambda: gemm(A, B, C, group_size_m=args.group_size, **pt)  # noqa: E731
                 desc = {"impl": "gemm_f16", **pt, "group_size_m": args.group_size}

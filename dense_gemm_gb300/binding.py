@@ -51,6 +51,13 @@ def load_library():
     lib.gemm_f16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64,
                              i32, u32, vp]
     lib.gemm_f16.restype = ctypes.c_int
+    u64 = ctypes.c_uint64
+    lib.gemm_f16_splitk.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                    i32, vp, u64, i32, u32, vp]
+    lib.gemm_f16_splitk.restype = ctypes.c_int
+    lib.gemm_f16_splitk_workspace_size.argtypes = [i64, i64, i64, i32, ctypes.POINTER(u64),
+                                                   ctypes.POINTER(i32)]
+    lib.gemm_f16_splitk_workspace_size.restype = ctypes.c_int
     lib.gemm_f16_tile_map.argtypes = [i32, i32, i32, u32, i32, vp, vp]
     lib.gemm_f16_tile_map.restype = ctypes.c_int
     lib.gemm_f16_get_config.argtypes = [i64, i64, u32, pi32, pi32, pi32, pi32, pi32]
@@ -132,6 +139,54 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
     return out
 
 
+def _check_operands(A, B, out):
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError(f"shapes {tuple(A.shape)} @ {tuple(B.shape)} do not chain")
+    if not (A.is_cuda and B.is_cuda):
+        raise ValueError("A and B must be CUDA tensors")
+    M, N = A.shape[0], B.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
+        raise ValueError("out must be a float32 CUDA tensor of shape [M, N]")
+    return out
+
+
+def splitk_workspace_size(M: int, N: int, K: int, splits: int = 0):
+    """(bytes, splits used) of gemm_f16_splitk for these sizes."""
+    b, sp = ctypes.c_uint64(), ctypes.c_int32()
+    _check(load_library().gemm_f16_splitk_workspace_size(M, N, K, splits, ctypes.byref(b),
+                                                         ctypes.byref(sp)),
+           "gemm_f16_splitk_workspace_size")
+    return int(b.value), int(sp.value)
+
+
+def gemm_splitk(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *, splits: int = 0,
+                workspace: torch.Tensor = None, group_size_m: int = 8, grouped: bool = True,
+                cross_tile: bool = True, stream=None) -> torch.Tensor:
+    """C = A @ B with K split across CTA pairs (gemm_f16_splitk). ``workspace``
+    (a CUDA tensor of at least splitk_workspace_size() bytes) is allocated
+    when omitted."""
+    out = _check_operands(A, B, out)
+    M, K = A.shape
+    N = B.shape[1]
+    need, _ = splitk_workspace_size(M, N, K, splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    sam, sak = A.stride()
+    sbk, sbn = B.stride()
+    scm, scn = out.stride()
+    st = load_library().gemm_f16_splitk(
+        A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1), max(sbk, 1),
+        max(sbn, 1), max(scm, 1), max(scn, 1), splits, workspace.data_ptr(), ws_bytes, group_size_m,
+        sched_flags(grouped, cross_tile), _stream_handle(stream))
+    _check(st, "gemm_f16_splitk")
+    return out
+
+
 def tile_map(num_m_tiles: int, num_n_tiles: int, group_size_m: int, grouped: bool,
              grid: int, device=None, stream=None) -> torch.Tensor:
     """[T, 3] int32 CUDA tensor from the kernel's scheduler: row tile_id =
@@ -203,3 +258,56 @@ def gemm_from_host(A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Ten
              cross_tile=cross_tile, single_cta=single_cta, stream=s)
         C_host.copy_(C_dev, non_blocking=True)
     return C_host
+
+
+class HostPipeline:
+    """Back-to-back GEMMs on host operands with the copies of consecutive calls
+    overlapped.
+
+    Each ``submit(A_host, B_host, C_host)`` copies A and B (pinned host fp16) to
+    one of ``depth`` device buffer sets, runs gemm_f16 there, and copies C back
+    into ``C_host`` (pinned fp32). Uploads and the GEMM run on one stream,
+    downloads on another, so the download of call i overlaps the upload and
+    GEMM of call i+1 (the host link carries both directions at once). A buffer
+    set is reused only after its previous download has finished. Call
+    ``synchronize()`` before reading the last ``C_host``.
+    """
+
+    def __init__(self, A_like: torch.Tensor, B_like: torch.Tensor, depth: int = 2, *,
+                 group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
+                 single_cta: bool = False, device=None):
+        device = torch.device(device or "cuda")
+        M, N = A_like.shape[0], B_like.shape[1]
+        self.kw = dict(group_size_m=group_size_m, grouped=grouped, cross_tile=cross_tile,
+                       single_cta=single_cta)
+        self.sets = [(torch.empty_strided(A_like.shape, A_like.stride(), dtype=A_like.dtype, device=device),
+                      torch.empty_strided(B_like.shape, B_like.stride(), dtype=B_like.dtype, device=device),
+                      torch.empty((M, N), dtype=torch.float32, device=device)) for _ in range(depth)]
+        self.s_in = torch.cuda.Stream(device=device)
+        self.s_out = torch.cuda.Stream(device=device)
+        self.gemm_done = [torch.cuda.Event() for _ in range(depth)]
+        self.out_done = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+        self.calls = 0
+
+    def submit(self, A_host: torch.Tensor, B_host: torch.Tensor, C_host: torch.Tensor):
+        j = self.calls % len(self.sets)
+        A_dev, B_dev, C_dev = self.sets[j]
+        with torch.cuda.stream(self.s_in):
+            if self.used[j]:
+                self.s_in.wait_event(self.out_done[j])  # C_dev[j] has been downloaded
+            A_dev.copy_(A_host, non_blocking=True)
+            B_dev.copy_(B_host, non_blocking=True)
+            gemm(A_dev, B_dev, C_dev, stream=self.s_in, **self.kw)
+            self.gemm_done[j].record(self.s_in)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.gemm_done[j])
+            C_host.copy_(C_dev, non_blocking=True)
+            self.out_done[j].record(self.s_out)
+        self.used[j] = True
+        self.calls += 1
+        return C_host
+
+    def synchronize(self):
+        self.s_in.synchronize()
+        self.s_out.synchronize()

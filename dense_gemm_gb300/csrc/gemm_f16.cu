@@ -124,6 +124,22 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D tiled tensor map (inner first) with a box of depth 1 in the outermost
+// dimension: the split-K workspace [S][M][ldw], so that TMA clips each slice on
+// its own M and N edges.
+bool encode_3d_f32(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // TMA can describe an operand whose contiguous extent is `inner` and whose other
@@ -156,6 +172,30 @@ void tile_shape(uint32_t flags, int *bm, int *bn) {
     *bn = single ? BN : pair::TILE_N;
 }
 
+// Split-K plan: kb_per_split k-blocks per slice and the number of non-empty
+// slices. `requested` == 0 picks enough slices to give every co-resident CTA
+// pair a unit (at most 32, at least one k-block per slice).
+struct SplitPlan {
+    int32_t splits;
+    int32_t kb_per_split;
+    int64_t ldw;  // workspace row stride (elements), N rounded up to 4
+};
+
+SplitPlan plan_splits(int64_t M, int64_t N, int64_t K, int32_t requested, int max_pairs) {
+    SplitPlan sp;
+    const int64_t num_kb = cdiv(K, BK);
+    const int64_t tiles = cdiv(M, pair::TILE_M) * cdiv(N, pair::TILE_N);
+    int64_t want = requested;
+    if (want <= 0) want = tiles >= max_pairs ? 1 : cdiv(max_pairs, tiles);
+    if (want > 32) want = 32;
+    if (want > num_kb) want = num_kb;
+    if (want < 1) want = 1;
+    sp.kb_per_split = int32_t(cdiv(num_kb, want));
+    sp.splits = int32_t(cdiv(num_kb, sp.kb_per_split));
+    sp.ldw = (N + 3) / 4 * 4;
+    return sp;
+}
+
 uint32_t next_epoch() {
     uint32_t e = g_epoch.fetch_add(1) + 1;
     if (e == 0) e = g_epoch.fetch_add(1) + 1;  // 0 means "no abort"
@@ -183,10 +223,23 @@ gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns) {
     return GEMM_OK;
 }
 
-gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
-                       int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
-                       int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
-                       uint32_t schedule_flags, gemm_stream_t stream_) {
+}  // extern "C"
+
+namespace {
+
+// Split-K request of one call: requested slices (0 = automatic) and the
+// caller's fp32 workspace.
+struct SplitReq {
+    bool enabled = false;
+    int32_t splits = 1;
+    void *workspace = nullptr;
+    uint64_t workspace_bytes = 0;
+};
+
+gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                        int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                        int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
+                        uint32_t schedule_flags, gemm_stream_t stream_, const SplitReq &sk) {
     // ---- validation (no GPU work before this point)
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_ARG;
@@ -227,6 +280,7 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
     const bool store_tma = tma_ok(C, N, stride_cm, 4);
     // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
     const bool use_pair = load_tma && !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
+    if (sk.enabled && !use_pair) return GEMM_ERR_UNSUPPORTED;  // split-K runs on CTA pairs with TMA loads
     const int tile_m = use_pair ? pair::TILE_M : BM;
     const int tile_n = use_pair ? pair::TILE_N : BN;
     const int cta_m = use_pair ? pair::CTA_M : BM;    // A rows one CTA loads
@@ -249,7 +303,20 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
                                          MN_CHUNK, BK);
         if (!okA || !okB) return GEMM_ERR_CUDA;
     }
-    if (store_tma) {
+    SplitPlan sp{1, int32_t(cdiv(K, BK)), N};
+    if (sk.enabled) {
+        sp = plan_splits(M, N, K, sk.splits, ds->max_pairs);
+        if (sp.splits > 1) {
+            const uint64_t need = uint64_t(sp.splits) * uint64_t(M) * uint64_t(sp.ldw) * 4u;
+            if (sk.workspace == nullptr || sk.workspace_bytes < need || !aligned16(sk.workspace))
+                return GEMM_ERR_INVALID_ARG;
+            if (!encode_3d_f32(&tmC, sk.workspace, uint64_t(N), uint64_t(M), uint64_t(sp.splits),
+                               uint64_t(sp.ldw) * 4u, uint64_t(M) * uint64_t(sp.ldw) * 4u, EPI_COLS, 32))
+                return GEMM_ERR_CUDA;
+        }
+    }
+    const bool split = sp.splits > 1;
+    if (!split && store_tma) {
         if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, stride_cm * 4, EPI_COLS, 32))
             return GEMM_ERR_CUDA;
     }
@@ -273,10 +340,19 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
     p.sched.grouped = grouped ? 1 : 0;
     p.num_tiles = int32_t(nm * nn);
     p.num_kb = int32_t(cdiv(K, BK));
+    p.splits = sp.splits;
+    p.kb_per_split = split ? sp.kb_per_split : p.num_kb;
+    if (int64_t(p.num_tiles) * sp.splits > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+    p.num_units = p.num_tiles * sp.splits;
     p.a_mn = a_k ? 0u : 1u;
     p.b_mn = b_n ? 1u : 0u;
     p.idesc = make_idesc(p.a_mn, p.b_mn, use_pair ? 2 * pair::CTA_M : BM, tile_n);
     p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
+    if (!use_pair) {  // the one-CTA kernel walks whole tiles
+        p.splits = 1;
+        p.kb_per_split = p.num_kb;
+        p.num_units = p.num_tiles;
+    }
     // C is written once and never read again: its stores carry an evict-first
     // L2 policy. Operand loads keep the default policy (an evict-last hint on
     // them measured slower: tensor-pipe activity 86.3 % -> 83.7 % at 16384^2).
@@ -285,28 +361,86 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
     p.wait.epoch = next_epoch();
 
     const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT);
-    const int programs = !persistent ? p.num_tiles : use_pair ? ds->max_pairs : ds->num_sms;
-    const int grid_programs = int(p.num_tiles < programs ? p.num_tiles : programs);
+    const int programs = !persistent ? p.num_units : use_pair ? ds->max_pairs : ds->num_sms;
+    const int grid_programs = int(p.num_units < programs ? p.num_units : programs);
     if (use_pair && int64_t(grid_programs) * 2 > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     const int grid = use_pair ? 2 * grid_programs : grid_programs;
     if (log_enabled())
         std::fprintf(stderr,
                      "[gemm_f16] M=%lld N=%lld K=%lld kernel=%s tiles=%d grid=%d load=%s store=%s A=%s "
-                     "B=%s order=%s G=%d cross_tile=%u persistent=%d\n",
+                     "B=%s order=%s G=%d cross_tile=%u persistent=%d splits=%d\n",
                      (long long)M, (long long)N, (long long)K, use_pair ? "cta-pair 256x256" : "one-cta 128x256",
                      p.num_tiles, grid,
                      load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
                      p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
-                     grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile, int(persistent));
+                     grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile, int(persistent),
+                     sp.splits);
 
     cudaError_t e;
-    if (use_pair) e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
-                                : launch_pair<false>(tmA, tmB, tmC, p, grid, stream);
+    if (split) {
+        e = launch_pair<true>(tmA, tmB, tmC, p, grid, stream);
+        if (e == cudaSuccess) {
+            const int64_t quads = M * ((N + 3) / 4);
+            const int threads = 256;
+            const int64_t want = cdiv(quads, threads);
+            const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
+            splitk_reduce_kernel<<<blocks, threads, 0, stream>>>(static_cast<const float *>(sk.workspace), C, M, N,
+                                                              sp.ldw, stride_cm, sp.splits);
+            e = cudaGetLastError();
+        }
+    } else if (use_pair)
+        e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
+                      : launch_pair<false>(tmA, tmB, tmC, p, grid, stream);
     else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, grid, stream);
     else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, grid, stream);
     else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, grid, stream);
     else e = launch<false, false>(tmA, tmB, tmC, p, grid, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                       int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                       int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
+                       uint32_t schedule_flags, gemm_stream_t stream) {
+    return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
+                     group_size_m, schedule_flags, stream, SplitReq());
+}
+
+gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int32_t splits,
+                                             uint64_t *bytes, int32_t *splits_used) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim || splits < 0)
+        return GEMM_ERR_INVALID_ARG;
+    int max_pairs = 1;
+    if (splits == 0 && M > 0 && N > 0 && K > 0) {
+        int dev = 0;
+        DeviceState *ds = nullptr;
+        if (cudaGetDevice(&dev) != cudaSuccess || device_init(dev, &ds) != cudaSuccess) return GEMM_ERR_CUDA;
+        max_pairs = ds->max_pairs;
+    }
+    SplitPlan sp{1, 1, (N + 3) / 4 * 4};
+    if (M > 0 && N > 0 && K > 0) sp = plan_splits(M, N, K, splits, max_pairs);
+    if (bytes) *bytes = sp.splits > 1 ? uint64_t(sp.splits) * uint64_t(M) * uint64_t(sp.ldw) * 4u : 0u;
+    if (splits_used) *splits_used = sp.splits;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_splitk(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                              int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                              int64_t stride_cm, int64_t stride_cn, int32_t splits, void *workspace,
+                              uint64_t workspace_bytes, int32_t group_size_m, uint32_t schedule_flags,
+                              gemm_stream_t stream) {
+    if (splits < 0) return GEMM_ERR_INVALID_ARG;
+    SplitReq sk;
+    sk.enabled = true;
+    sk.splits = splits;
+    sk.workspace = workspace;
+    sk.workspace_bytes = workspace_bytes;
+    return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
+                     group_size_m, schedule_flags, stream, sk);
 }
 
 gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles, int32_t group_size_m,

@@ -176,6 +176,13 @@ struct Params {
     Sched sched;
     int32_t num_tiles;
     int32_t num_kb;     // cdiv(K, BK) >= 1
+    // Split-K (CTA-pair kernel only): work unit u covers tile u % num_tiles and
+    // k-blocks [s * kb_per_split, min(num_kb, (s + 1) * kb_per_split)) with
+    // s = u / num_tiles; with splits > 1 the epilogue stores the partial tile into
+    // slice s of the workspace (3-D tensor map in place of C's) instead of C.
+    int32_t splits;     // >= 1
+    int32_t kb_per_split;
+    int32_t num_units;  // num_tiles * splits
     uint32_t a_mn;      // 1: A is M-major in memory (and in shared memory)
     uint32_t b_mn;      // 1: B is N-major
     uint32_t idesc;     // tcgen05 instruction descriptor
@@ -286,7 +293,8 @@ __device__ __forceinline__ void load_operand_tile(uint32_t dst, const uint16_t *
 template <bool kTmaStore, typename Drained>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int64_t col_base,
                                               const Params &p, const CUtensorMap *tmC, uint32_t stg,
-                                              uint32_t &buf, int lane, Drained drained) {
+                                              uint32_t &buf, int lane, Drained drained,
+                                              int32_t split = 0) {
 #pragma unroll 1
     for (int c = 0; c < BN / EPI_COLS; ++c) {
         uint32_t v[32];
@@ -305,7 +313,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
             __syncwarp();
             if (lane == 0) {
                 if (row0 < p.M && col0 < p.N) {
-                    if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
+                    if (p.splits > 1)  // partial tile -> workspace slice `split`, read once by the reduction
+                        tma_store_3d_hint(tmC, dst, int32_t(col0), int32_t(row0), split,
+                                          l2_policy_evict_normal());
+                    else if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
                         tma_store_2d_hint(tmC, dst, int32_t(col0), int32_t(row0), l2_policy_evict_first());
                     else
                         tma_store_2d(tmC, dst, int32_t(col0), int32_t(row0));
@@ -562,6 +573,39 @@ __global__ void tile_map_kernel(Sched s, int32_t num_tiles, int32_t *out) {
         out[3 * int64_t(t) + 0] = int32_t(blockIdx.x);
         out[3 * int64_t(t) + 1] = tm;
         out[3 * int64_t(t) + 2] = tn;
+    }
+}
+
+// Split-K reduction: C[i][j] = sum over s = 0 .. S-1, in that order, of
+// W[s][i][j] (W dense [S][M][ldw] fp32). Fixed order: the result does not
+// depend on scheduling. Four consecutive columns per thread.
+__global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C, int64_t M,
+                                     int64_t N, int64_t ldw, int64_t scm, int32_t S) {
+    const int64_t nq = (N + 3) / 4;
+    const int64_t total = M * nq;
+    const int64_t slice = M * ldw;
+    const bool vec_c = (scm % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t i = e / nq, j = (e - i * nq) * 4;
+        const float *w = W + i * ldw + j;
+        float4 acc = *reinterpret_cast<const float4 *>(w);  // ldw % 4 == 0, W 16-byte aligned
+        for (int32_t s = 1; s < S; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(w + s * slice);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        float *c = C + i * scm + j;
+        if (vec_c && j + 3 < N) {
+            *reinterpret_cast<float4 *>(c) = acc;
+        } else {
+            c[0] = acc.x;
+            if (j + 1 < N) c[1] = acc.y;
+            if (j + 2 < N) c[2] = acc.z;
+            if (j + 3 < N) c[3] = acc.w;
+        }
     }
 }
 

@@ -108,16 +108,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             int32_t it = 0;
-            for (int32_t tile = pair_id; ok && tile < p.num_tiles; tile += num_pairs, ++it) {
+            for (int32_t u = pair_id; ok && u < p.num_units; u += num_pairs, ++it) {
+                const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
+                const int32_t kb0 = split * p.kb_per_split;
+                const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
                 int32_t tm, tn;
                 tile_coords(tile, p.sched, tm, tn);
                 if (!p.cross_tile && it > 0) {
-                    const int32_t j = it - 1;  // this CTA's epilogue has drained tile j
+                    const int32_t j = it - 1;  // this CTA's epilogue has drained unit j
                     if (!mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
                 }
                 const int32_t m0 = tm * pair::TILE_M + int32_t(rank) * pair::CTA_M;
                 const int32_t n0 = tn * pair::TILE_N + int32_t(rank) * pair::CTA_N;
-                for (int32_t kb = 0; kb < num_kb; ++kb) {
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair::PAIR_TX_BYTES);
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
@@ -190,7 +193,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
             const DescStep da = make_desc_step(sA, p.a_mn, pair::A_STAGE_BYTES);
             const DescStep db = make_desc_step(sB, p.b_mn, pair::B_STAGE_BYTES);
             const uint32_t idesc = p.idesc;
-            for (int32_t tile = pair_id; ok && tile < p.num_tiles; tile += num_pairs, ++it) {
+            for (int32_t u = pair_id; ok && u < p.num_units; u += num_pairs, ++it) {
+                const int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
+                const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
                 const uint32_t acc = it & 1, use = it >> 1;
                 // both CTAs' epilogues have released this accumulator (remote arrivals)
                 if (!__all_sync(0xffffffffu,
@@ -200,7 +205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * pair::TILE_N;
-                for (int32_t kb = 0; kb < num_kb; ++kb) {
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
                     if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.wait))) {
                         ok = false;
                         break;
@@ -211,7 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
 #pragma unroll
                     for (int k16 = 0; k16 < BK / UMMA_K; ++k16)
                         mma_f16_pair_elect(d_tmem, a0 + k16 * da.k16, b0 + k16 * db.k16, idesc,
-                                           (kb | k16) != 0 ? 1u : 0u);
+                                           ((kb - kb0) | k16) != 0 ? 1u : 0u);
                     mma_commit_pair_mc_elect(empty_bar(stage), 0x3);  // both CTAs' slots reusable
                     if (++stage == pair::STAGES) { stage = 0; phase ^= 1u; }
                 }
@@ -228,7 +233,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         const uint32_t stg = base + pair::OFF_EPI + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         uint32_t buf = 0;
         int32_t it = 0;
-        for (int32_t tile = pair_id; tile < p.num_tiles; tile += num_pairs, ++it) {
+        for (int32_t u = pair_id; u < p.num_units; u += num_pairs, ++it) {
+            const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
             int32_t tm, tn;
             tile_coords(tile, p.sched, tm, tn);
             const uint32_t acc = it & 1, use = it >> 1;
@@ -244,7 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                     mbar_arrive(tdone_bar(acc));
                     mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
                 }
-            });
+            }, split);
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -361,3 +361,17 @@ __device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar) {
 }
 
 }  // namespace g16
+
+// ---------------------------------------------------------------- 3-D TMA store
+namespace g16 {
+
+__device__ __forceinline__ void tma_store_3d_hint(const void *tmap, uint32_t src, int32_t x, int32_t y,
+                                                  int32_t z, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+            tmap),
+        "r"(x), "r"(y), "r"(z), "r"(src), "l"(pol)
+        : "memory");
+}
+
+}  // namespace g16

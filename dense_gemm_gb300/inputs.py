@@ -99,6 +99,9 @@ WORKLOADS = {
                                       b_layout="col", seed=1050, tags=("ragged",)),
     "ragged_8191x8191x257": Workload("ragged_8191x8191x257", 8191, 8191, 257, "uniform",
                                      b_layout="col", seed=1060, tags=("ragged",)),
+    # few output tiles, long K: the case split-K is for (not one of the pages' shapes)
+    "longk_1024x1024x32768": Workload("longk_1024x1024x32768", 1024, 1024, 32768, "uniform",
+                                      seed=1070, tags=("study",)),
 }
 
 HEADLINE = "square_16384x16384x4096"

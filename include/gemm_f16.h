@@ -105,6 +105,44 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C,
                        gemm_stream_t stream);
 
 /*
+ * gemm_f16_splitk — C = A @ B with the K dimension split across CTA pairs
+ * (for problems with fewer output tiles than CTA pairs, e.g. small M x N with
+ * long K). The pages name Stream-K as a later step without describing it
+ * ([persistent] "naive persistent matmul"); this is its plain split-K form.
+ *
+ * Same arguments, layouts and semantics as gemm_f16, plus:
+ * splits: requested K slices (>= 1), or 0 to choose: enough slices to give
+ *   every co-resident CTA pair a unit, at most 32. The count used never gives
+ *   a slice zero k-blocks (see gemm_f16_splitk_workspace_size).
+ * workspace: DEVICE buffer owned by the caller, 16-byte aligned, of at least
+ *   gemm_f16_splitk_workspace_size() bytes (may be NULL when that size is 0).
+ * Work unit u computes tile u % T over slice u / T into workspace[slice]
+ * (fp32, [slices][M][round_up(N, 4)]); a second kernel on the same stream then
+ * sums the slices into C in slice order 0, 1, ... (deterministic). The
+ * workspace must not be used by another call that overlaps on the GPU.
+ * Needs TMA-loadable A and B (see gemm_f16); otherwise, or with
+ * GEMM_SCHED_SINGLE_CTA, returns GEMM_ERR_UNSUPPORTED. A workspace smaller
+ * than required, or misaligned -> GEMM_ERR_INVALID_ARG.
+ */
+gemm_status_t gemm_f16_splitk(const void *A, const void *B, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t stride_am, int64_t stride_ak,
+                              int64_t stride_bk, int64_t stride_bn,
+                              int64_t stride_cm, int64_t stride_cn,
+                              int32_t splits, void *workspace, uint64_t workspace_bytes,
+                              int32_t group_size_m, uint32_t schedule_flags,
+                              gemm_stream_t stream);
+
+/*
+ * gemm_f16_splitk_workspace_size — workspace bytes and slice count that
+ * gemm_f16_splitk will use for these sizes and `splits` (0 = automatic, which
+ * needs a device). *bytes is 0 when one slice is used (no workspace needed).
+ * Either output may be NULL.
+ */
+gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int32_t splits,
+                                             uint64_t *bytes, int32_t *splits_used);
+
+/*
  * gemm_f16_tile_map — the kernel's own tile scheduler, run on the GPU.
  *
  * Defined by [persistent] "naive persistent matmul" (visiting order) and

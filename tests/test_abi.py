@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert "gemm_f16" in names and "gemm_f16_tile_map" in names
-    assert len(names) == 8, names
+    assert len(names) == 10, names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -127,3 +127,21 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "oracle_gemm" not in text, f
+
+
+def test_splitk_host_validation(lib):
+    import ctypes as C
+    b, sp = C.c_uint64(), C.c_int32()
+    assert lib.gemm_f16_splitk_workspace_size(512, 512, 512, 4, C.byref(b), C.byref(sp)) == 0
+    assert sp.value == 4 and b.value == 4 * 512 * 512 * 4
+    # never an empty slice: 5 k-blocks asked for 4 slices -> 2 per slice -> 3 slices
+    assert lib.gemm_f16_splitk_workspace_size(300, 301, 320, 4, C.byref(b), C.byref(sp)) == 0
+    assert sp.value == 3 and b.value == 3 * 300 * 304 * 4
+    assert lib.gemm_f16_splitk_workspace_size(512, 512, 64, 8, C.byref(b), C.byref(sp)) == 0
+    assert sp.value == 1 and b.value == 0
+    assert lib.gemm_f16_splitk_workspace_size(-1, 512, 64, 8, None, None) == 1
+    assert lib.gemm_f16_splitk_workspace_size(4, 512, 64, -1, None, None) == 1
+    a = dict(A=16, B=16, C=16, M=4, N=4, K=4, sam=4, sak=1, sbk=4, sbn=1, scm=4, scn=1)
+    args = [a[k] for k in ("A", "B", "C", "M", "N", "K", "sam", "sak", "sbk", "sbn", "scm", "scn")]
+    assert lib.gemm_f16_splitk(*args, -1, None, 0, 8, 3, None) == 1
+    assert lib.gemm_f16_splitk(*args[:3], 0, *args[4:], 4, None, 0, 8, 3, None) == 0  # M == 0

@@ -313,3 +313,81 @@ def test_bounded_wait_times_out_and_context_survives():
     A = draw(300, 200, "int", 99)
     B = draw(200, 400, "int", 98)
     assert np.array_equal(run(A, B)[1], oracle.gemm(A, B))
+
+
+# ------------------------------------------------------------------ host-operand APIs
+
+def test_gemm_from_host_matches_oracle():
+    from dense_gemm_gb300 import gemm_from_host
+    A = draw(300, 200, "int", 111).pin_memory()
+    B = draw(200, 500, "int", 112).pin_memory()
+    C = gemm_from_host(A, B)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.numpy().astype(np.float64), oracle.gemm(A, B))
+
+
+def test_host_pipeline_overlapped_calls_match_oracle():
+    from dense_gemm_gb300 import HostPipeline
+    inputs = [(draw(384, 256, "int", 120 + i).pin_memory(), draw(256, 640, "int", 140 + i).pin_memory())
+              for i in range(5)]
+    outs = [torch.empty((384, 640), dtype=torch.float32, pin_memory=True) for _ in inputs]
+    pipe = HostPipeline(inputs[0][0], inputs[0][1], depth=2)
+    for (A, B), C in zip(inputs, outs):
+        pipe.submit(A, B, C)
+    pipe.synchronize()
+    for (A, B), C in zip(inputs, outs):
+        assert np.array_equal(C.numpy().astype(np.float64), oracle.gemm(A, B))
+
+
+# ------------------------------------------------------------------ split-K (scratch workspace)
+
+@pytest.mark.parametrize("shape", [(512, 512, 512), (300, 304, 320), (256, 256, 64), (129, 704, 1000),
+                                   (1024, 512, 4096)])
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 7])
+def test_splitk_integer_bit_exact(shape, splits):
+    from dense_gemm_gb300 import gemm_splitk
+    M, N, K = shape
+    A = draw(M, K, "int", 200 + M)
+    B = draw(K, N, "int", 201 + N)
+    C = gemm_splitk(to_dev(A), to_dev(B), splits=splits)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), oracle.gemm(A, B))
+
+
+@pytest.mark.parametrize("grouped,cross", ORDERS)
+def test_splitk_random_within_bound_and_strided_c(grouped, cross):
+    from dense_gemm_gb300 import gemm_splitk
+    M, N, K = 384, 520, 2000
+    A = draw(M, K, "normal", 210)
+    B = relayout(draw(K, N, "normal", 211), "col")
+    ref = oracle.gemm(A, B)
+    buf = torch.full((M * 531 + 1,), float("nan"), device="cuda")
+    C = buf.as_strided((M, N), (531, 1), 1)  # odd stride, misaligned base
+    gemm_splitk(to_dev(A), to_dev(B), C, splits=5, grouped=grouped, cross_tile=cross)
+    torch.cuda.synchronize()
+    assert_within_bound(C.cpu().numpy().astype(np.float64), ref, A, B, "split-K")
+
+
+def test_splitk_matches_unsplit_on_integers_full_512():
+    from dense_gemm_gb300 import gemm_splitk, splitk_workspace_size
+    w = WORKLOADS["square_512"]
+    A, B = w.operands()
+    ref = oracle.gemm(A, B)
+    need, used = splitk_workspace_size(512, 512, 512, 0)
+    assert used > 1 and need == used * 512 * 512 * 4
+    C = gemm_splitk(to_dev(A), to_dev(B))
+    torch.cuda.synchronize()
+    assert_within_bound(C.cpu().numpy().astype(np.float64), ref, A, B, "512^3 split-K")
+
+
+def test_splitk_rejects_small_workspace_and_unaligned_operands():
+    from dense_gemm_gb300 import gemm_splitk
+    A = torch.ones(512, 512, dtype=torch.float16, device="cuda")
+    with pytest.raises(GemmError) as e:
+        gemm_splitk(A, A, splits=4, workspace=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == 1
+    A2 = to_dev(relayout(draw(300, 257, "int", 5), "row"))  # 514-byte rows: no TMA
+    B2 = to_dev(draw(257, 300, "int", 6))
+    with pytest.raises(GemmError) as e:
+        gemm_splitk(A2, B2, splits=2)
+    assert e.value.status == 2
