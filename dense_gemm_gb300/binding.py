@@ -58,6 +58,9 @@ def load_library():
     lib.gemm_f16_splitk_workspace_size.argtypes = [i64, i64, i64, i32, ctypes.POINTER(u64),
                                                    ctypes.POINTER(i32)]
     lib.gemm_f16_splitk_workspace_size.restype = ctypes.c_int
+    lib.gemm_f16_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
+                                            i64, i32, i32, u32, vp]
+    lib.gemm_f16_splitk_noalloc.restype = ctypes.c_int
     lib.gemm_f16_tile_map.argtypes = [i32, i32, i32, u32, i32, vp, vp]
     lib.gemm_f16_tile_map.restype = ctypes.c_int
     lib.gemm_f16_get_config.argtypes = [i64, i64, u32, pi32, pi32, pi32, pi32, pi32]
@@ -184,6 +187,26 @@ def gemm_splitk(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *, s
         max(sbn, 1), max(scm, 1), max(scn, 1), splits, workspace.data_ptr(), ws_bytes, group_size_m,
         sched_flags(grouped, cross_tile), _stream_handle(stream))
     _check(st, "gemm_f16_splitk")
+    return out
+
+
+def gemm_splitk_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, *, splits: int = 0,
+                        group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
+                        stream=None) -> torch.Tensor:
+    """gemm_f16_splitk_noalloc: split-K through the library's built-in 32 MiB
+    scratch, for callers that cannot allocate device memory at this point
+    (``out`` must be given; nothing is allocated)."""
+    out = _check_operands(A, B, out)
+    M, K = A.shape
+    N = B.shape[1]
+    sam, sak = A.stride()
+    sbk, sbn = B.stride()
+    scm, scn = out.stride()
+    st = load_library().gemm_f16_splitk_noalloc(
+        A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1),
+        max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1), splits, group_size_m,
+        sched_flags(grouped, cross_tile), _stream_handle(stream))
+    _check(st, "gemm_f16_splitk_noalloc")
     return out
 
 

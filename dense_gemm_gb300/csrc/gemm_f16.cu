@@ -531,3 +531,53 @@ gemm_status_t gemm_f16_sync_status(gemm_stream_t stream_) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Split-K without any device allocation: the workspace is a fixed array in the
+// library image instead of caller memory. Meant for callers that cannot call
+// cudaMalloc at the point where they multiply: their device memory is owned by
+// another allocator or a fixed arena, or they cannot afford the device-wide
+// synchronisation and the failure modes of an allocation on that path.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr uint64_t kNoAllocScratchBytes = 32ull << 20;  // 32 MiB, held by every device that loads the library
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct ScratchState {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    void *ptr = nullptr;
+};
+ScratchState g_scratch[kMaxDevices];
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_f16_splitk_noalloc(const void *A, const void *B, float *C, int64_t M,
+                                                 int64_t N, int64_t K, int64_t stride_am,
+                                                 int64_t stride_ak, int64_t stride_bk,
+                                                 int64_t stride_bn, int64_t stride_cm,
+                                                 int64_t stride_cn, int32_t splits,
+                                                 int32_t group_size_m, uint32_t schedule_flags,
+                                                 gemm_stream_t stream) {
+    uint64_t need = 0;
+    int32_t used = 1;
+    const gemm_status_t st = gemm_f16_splitk_workspace_size(M, N, K, splits, &need, &used);
+    if (st != GEMM_OK) return st;
+    if (need > kNoAllocScratchBytes) return GEMM_ERR_UNSUPPORTED;  // larger than the built-in scratch
+    void *ws = nullptr;
+    if (need > 0) {
+        // In host code the array's name is only a stand-in: its device address is
+        // looked up once per device, with that device current.
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+        ScratchState &s = g_scratch[dev];
+        std::call_once(s.once, [&s] { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
+        if (s.err != cudaSuccess || s.ptr == nullptr) return GEMM_ERR_CUDA;
+        ws = s.ptr;
+    }
+    return gemm_f16_splitk(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm,
+                           stride_cn, splits, ws, kNoAllocScratchBytes, group_size_m, schedule_flags,
+                           stream);
+}

@@ -143,6 +143,34 @@ gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, in
                                              uint64_t *bytes, int32_t *splits_used);
 
 /*
+ * gemm_f16_splitk_noalloc — gemm_f16_splitk with no device allocation at all.
+ * The pages have no counterpart to this entry point.
+ *
+ * For callers that must not allocate device memory where they multiply: their
+ * memory belongs to another allocator or a fixed arena, or they cannot take
+ * the device-wide synchronisation and out-of-memory failures that cudaMalloc
+ * brings on that path. Instead of a caller workspace it uses a 32 MiB array
+ * built into the library (every GPU that loads the library holds it until the
+ * process exits). Arguments as gemm_f16_splitk, without the workspace.
+ * - Problems whose split-K workspace (gemm_f16_splitk_workspace_size) exceeds
+ *   32 MiB are rejected with GEMM_ERR_UNSUPPORTED; nothing is launched.
+ * - The first call on a device that needs the scratch looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.
+ * - All calls share the one array and it keeps the last call's contents;
+ *   nothing in it needs to start at zero. Calls that overlap on the GPU (on
+ *   different streams, or from different threads) race on it: serialise them.
+ * - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+gemm_status_t gemm_f16_splitk_noalloc(const void *A, const void *B, float *C,
+                                      int64_t M, int64_t N, int64_t K,
+                                      int64_t stride_am, int64_t stride_ak,
+                                      int64_t stride_bk, int64_t stride_bn,
+                                      int64_t stride_cm, int64_t stride_cn,
+                                      int32_t splits, int32_t group_size_m,
+                                      uint32_t schedule_flags, gemm_stream_t stream);
+
+/*
  * gemm_f16_tile_map — the kernel's own tile scheduler, run on the GPU.
  *
  * Defined by [persistent] "naive persistent matmul" (visiting order) and
