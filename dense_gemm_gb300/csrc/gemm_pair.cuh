@@ -235,6 +235,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         int32_t it = 0;
         for (int32_t u = pair_id; u < p.num_units; u += num_pairs, ++it) {
             const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
+            const int32_t kb0 = split * p.kb_per_split;
+            const uint32_t pace = epilogue_pace_ns(min(num_kb, kb0 + p.kb_per_split) - kb0, p.cross_tile);
             int32_t tm, tn;
             tile_coords(tile, p.sched, tm, tn);
             const uint32_t acc = it & 1, use = it >> 1;
@@ -250,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                     mbar_arrive(tdone_bar(acc));
                     mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
                 }
-            }, split);
+            }, split, pace);
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();
