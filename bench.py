@@ -54,7 +54,8 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
-    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk"],
+    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
+                                       "outdtype"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
@@ -436,7 +437,9 @@ def run_sweep(args):
     cublas - context line: torch.matmul (cuBLAS, fp16 output) on 8192^2 and
              16384^2, K = 4096, next to gemm_f16 on the same operands;
     splitk - gemm_f16 vs gemm_f16_splitk (automatic slices) on 512^3 and
-             1024^2 x 32768 (fewer tiles than CTA pairs)."""
+             1024^2 x 32768 (fewer tiles than CTA pairs);
+    outdtype - fp32 vs fp16 vs bf16 C (gemm_f16_out) on the headline workload
+               and at K = 512, where the C store dominates the traffic."""
     import torch
     from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
@@ -448,6 +451,9 @@ def run_sweep(args):
     elif args.sweep == "ksweep":
         names = [n for n in WORKLOADS if n.startswith("ksweep_")]
         points = [dict(grouped=True, cross_tile=c, single_cta=False) for c in (True, False)]
+    elif args.sweep == "outdtype":
+        names = [HEADLINE, "ksweep_16384x16384x512"]
+        points = [("out", torch.float32), ("out", torch.float16), ("out", torch.bfloat16)]
     elif args.sweep == "splitk":
         names = ["square_512", "longk_1024x1024x32768"]
         points = [dict(grouped=True, cross_tile=True, single_cta=False), "splitk"]
@@ -468,7 +474,12 @@ def run_sweep(args):
         A, B = A_host.to(dev), B_host.to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
         for pt in points:
-            if pt == "torch.matmul":
+            if isinstance(pt, tuple) and pt[0] == "out":
+                Cx = torch.empty((w.M, w.N), dtype=pt[1], device=dev)
+                run = lambda: gemm(A, B, Cx, group_size_m=args.group_size)  # noqa: E731
+                desc = {"impl": "gemm_f16_out" if pt[1] != torch.float32 else "gemm_f16",
+                        "c_dtype": str(pt[1]).replace("torch.", "")}
+            elif pt == "torch.matmul":
                 run = lambda: torch.matmul(A, B)  # noqa: E731  (cuBLAS, fp16 output)
                 desc = {"impl": "torch.matmul (cuBLAS), fp16 output"}
             elif pt == "splitk":

@@ -61,6 +61,9 @@ def load_library():
     lib.gemm_f16_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
                                             i64, i32, i32, u32, vp]
     lib.gemm_f16_splitk_noalloc.restype = ctypes.c_int
+    lib.gemm_f16_out.argtypes = [vp, vp, vp, i32, ctypes.c_float, i64, i64, i64, i64, i64, i64,
+                                 i64, i64, i64, i32, u32, vp]
+    lib.gemm_f16_out.restype = ctypes.c_int
     lib.gemm_f16_tile_map.argtypes = [i32, i32, i32, u32, i32, vp, vp]
     lib.gemm_f16_tile_map.restype = ctypes.c_int
     lib.gemm_f16_get_config.argtypes = [i64, i64, u32, pi32, pi32, pi32, pi32, pi32]
@@ -110,13 +113,19 @@ def sched_flags(grouped: bool = True, cross_tile: bool = True, single_cta: bool 
             | (SCHED_SINGLE_CTA if single_cta else 0) | (0 if persistent else SCHED_NON_PERSISTENT))
 
 
+_OUT_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
 def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
          group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
-         single_cta: bool = False, persistent: bool = True, stream=None) -> torch.Tensor:
-    """C = A @ B with A [M,K], B [K,N] fp16 CUDA tensors; C fp32 [M,N].
+         single_cta: bool = False, persistent: bool = True, alpha: float = 1.0,
+         out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
+    """C = alpha * (A @ B) with A [M,K], B [K,N] fp16 CUDA tensors.
 
-    ``out`` (fp32, [M,N], unit column stride) is written if given, else
-    allocated. Strided views are passed through as strides.
+    ``out`` ([M,N], unit column stride, float32 / float16 / bfloat16) is
+    written if given, else allocated with ``out_dtype``. fp32 output with
+    alpha == 1 goes through gemm_f16, everything else through gemm_f16_out.
+    Strided views are passed through as strides.
     """
     if A.dtype != torch.float16 or B.dtype != torch.float16:
         raise TypeError("A and B must be float16")
@@ -127,18 +136,24 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
     M, K = A.shape
     N = B.shape[1]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
-    if out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
-        raise ValueError("out must be a float32 CUDA tensor of shape [M, N]")
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if out.dtype not in _OUT_CODES or tuple(out.shape) != (M, N) or not out.is_cuda:
+        raise ValueError("out must be a float32/float16/bfloat16 CUDA tensor of shape [M, N]")
     flags = sched_flags(grouped, cross_tile, single_cta, persistent)
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
     # torch gives stride 1 to size-1 dims' neighbours freely; keep them >= 1
-    st = gemm_raw(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K,
-                  max(sam, 1), max(sak, 1), max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1),
-                  group_size_m, flags, _stream_handle(stream))
-    _check(st, "gemm_f16")
+    strides = (max(sam, 1), max(sak, 1), max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1))
+    if out.dtype == torch.float32 and alpha == 1.0:
+        st = gemm_raw(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, *strides,
+                      group_size_m, flags, _stream_handle(stream))
+        _check(st, "gemm_f16")
+    else:
+        st = load_library().gemm_f16_out(A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                                         _OUT_CODES[out.dtype], float(alpha), M, N, K, *strides,
+                                         group_size_m, flags, _stream_handle(stream))
+        _check(st, "gemm_f16_out")
     return out
 
 

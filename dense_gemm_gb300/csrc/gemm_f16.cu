@@ -236,10 +236,13 @@ struct SplitReq {
     uint64_t workspace_bytes = 0;
 };
 
-gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                         int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
                         int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
-                        uint32_t schedule_flags, gemm_stream_t stream_, const SplitReq &sk) {
+                        uint32_t schedule_flags, gemm_stream_t stream_, const SplitReq &sk,
+                        uint32_t out_dtype = GEMM_OUT_F32, float alpha = 1.0f) {
+    if (out_dtype > GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
+    const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
     // ---- validation (no GPU work before this point)
     if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim)
         return GEMM_ERR_INVALID_ARG;
@@ -269,7 +272,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64
         const int threads = 256;
         const int64_t blocks64 = cdiv(total, threads);
         const int blocks = int(blocks64 < 8 * int64_t(ds->num_sms) ? blocks64 : 8 * int64_t(ds->num_sms));
-        zero_c_kernel<<<blocks, threads, 0, stream>>>(C, M, N, stride_cm);
+        zero_c_kernel<<<blocks, threads, 0, stream>>>(C, M, N, stride_cm, esize);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
@@ -277,7 +280,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64
     const bool a_tma = a_k ? tma_ok(A, K, stride_am, 2) : tma_ok(A, M, stride_ak, 2);
     const bool b_tma = b_n ? tma_ok(B, N, stride_bk, 2) : tma_ok(B, K, stride_bn, 2);
     const bool load_tma = a_tma && b_tma;
-    const bool store_tma = tma_ok(C, N, stride_cm, 4);
+    const bool store_tma = tma_ok(C, N, stride_cm, esize);
     // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
     const bool use_pair = load_tma && !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
     if (sk.enabled && !use_pair) return GEMM_ERR_UNSUPPORTED;  // split-K runs on CTA pairs with TMA loads
@@ -317,15 +320,21 @@ gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64
     }
     const bool split = sp.splits > 1;
     if (!split && store_tma) {
-        if (!encode_2d(&tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, C, N, M, stride_cm * 4, EPI_COLS, 32))
-            return GEMM_ERR_CUDA;
+        const CUtensorMapDataType dt = out_dtype == GEMM_OUT_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                       : out_dtype == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        // one 128-byte row of the box: 32 fp32 or 64 16-bit elements, 32 rows
+        if (!encode_2d(&tmC, dt, C, N, M, stride_cm * esize, 128 / esize, 32)) return GEMM_ERR_CUDA;
     }
 
     Params p;
     std::memset(&p, 0, sizeof(p));
     p.A = static_cast<const uint16_t *>(A);
     p.B = static_cast<const uint16_t *>(B);
-    p.C = C;
+    p.C = static_cast<float *>(C);
+    // split-K: the GEMM writes fp32 partials; the reduction scales and rounds
+    p.out_dtype = split ? uint32_t(GEMM_OUT_F32) : out_dtype;
+    p.alpha = split ? 1.0f : alpha;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -385,7 +394,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, float *C, int64_t M, int64
             const int64_t want = cdiv(quads, threads);
             const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
             splitk_reduce_kernel<<<blocks, threads, 0, stream>>>(static_cast<const float *>(sk.workspace), C, M, N,
-                                                              sp.ldw, stride_cm, sp.splits);
+                                                              sp.ldw, stride_cm, sp.splits, out_dtype, alpha);
             e = cudaGetLastError();
         }
     } else if (use_pair)
@@ -408,6 +417,15 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C, int64_t M, int64_
                        uint32_t schedule_flags, gemm_stream_t stream) {
     return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
                      group_size_m, schedule_flags, stream, SplitReq());
+}
+
+gemm_status_t gemm_f16_out(const void *A, const void *B, void *C, int32_t c_dtype, float alpha, int64_t M,
+                           int64_t N, int64_t K, int64_t stride_am, int64_t stride_ak, int64_t stride_bk,
+                           int64_t stride_bn, int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
+                           uint32_t schedule_flags, gemm_stream_t stream) {
+    if (c_dtype < GEMM_OUT_F32 || c_dtype > GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
+    return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
+                     group_size_m, schedule_flags, stream, SplitReq(), uint32_t(c_dtype), alpha);
 }
 
 gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int32_t splits,

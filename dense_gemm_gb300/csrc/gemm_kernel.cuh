@@ -29,6 +29,7 @@
 // (bounded) for its own copies in flight, and the CTA frees its TMEM and exits.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cstdint>
 
@@ -188,6 +189,8 @@ struct Params {
     uint32_t idesc;     // tcgen05 instruction descriptor
     uint32_t cross_tile;
     uint32_t l2_mode;   // bit 0: C stores evict-first; bit 1: A/B loads evict-last (pair kernel)
+    uint32_t out_dtype; // C element type: 0 fp32, 1 fp16, 2 bf16 (nearest-even)
+    float alpha;        // C = alpha * (A @ B)
     WaitCtl wait;
 };
 
@@ -314,6 +317,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
         tmem_ld_32x32b_x32(t_row + c * EPI_COLS, v);
         tmem_ld_wait();
         if (c == BN / EPI_COLS - 1) drained();
+        if (p.alpha != 1.0f) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(p.alpha * __uint_as_float(v[i]));
+        }
         const int64_t col0 = col_base + c * EPI_COLS;
         if (kTmaStore) {
             const uint32_t dst = stg + buf * EPI_BUF_BYTES;
@@ -350,6 +357,80 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
                 const uint32_t bits = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
                 const int64_t row = row0 + r;
                 if (row < p.M && col < p.N) p.C[row * p.scm + col] = __uint_as_float(bits);
+            }
+        }
+    }
+}
+
+// Two fp32 values -> one 32-bit word of two 16-bit values (lo in the low half),
+// each round-to-nearest-even to fp16 (dtype 1) or bf16 (dtype 2).
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, uint32_t dtype) {
+    if (dtype == 1) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+// 16-bit C: like epilogue_tile, but 64 columns per chunk (two 32-column TMEM
+// loads), scaled by alpha and rounded, so that each staging row is again 128
+// bytes; the TMA store box is 64 x 32 elements of the 16-bit type.
+template <bool kTmaStore, typename Drained>
+__device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, int64_t col_base,
+                                                const Params &p, const CUtensorMap *tmC, uint32_t stg,
+                                                uint32_t &buf, int lane, Drained drained,
+                                                uint32_t pace_ns = 0) {
+    const float alpha = p.alpha;
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+        uint32_t v[32], w[32];
+        tmem_ld_32x32b_x32(t_row + c * 64, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[i] = pack_16x2(alpha * __uint_as_float(v[2 * i]), alpha * __uint_as_float(v[2 * i + 1]),
+                             p.out_dtype);
+        tmem_ld_32x32b_x32(t_row + c * 64 + 32, v);
+        tmem_ld_wait();
+        if (c == BN / 64 - 1) drained();
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            w[16 + i] = pack_16x2(alpha * __uint_as_float(v[2 * i]),
+                                  alpha * __uint_as_float(v[2 * i + 1]), p.out_dtype);
+        const int64_t col0 = col_base + c * 64;
+        if (kTmaStore) {
+            const uint32_t dst = stg + buf * EPI_BUF_BYTES;
+            if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(dst + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (row0 < p.M && col0 < p.N)
+                    tma_store_2d_hint(tmC, dst, int32_t(col0), int32_t(row0), l2_policy_evict_first());
+                bulk_commit_group();
+            }
+            buf ^= 1u;
+            if (pace_ns != 0 && c < BN / 64 - 1) __nanosleep(pace_ns);
+        } else {
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+            __syncwarp();
+            const int64_t col = col0 + 2 * lane;  // this lane: columns col, col + 1
+            uint16_t *C16 = reinterpret_cast<uint16_t *>(p.C);
+#pragma unroll 4
+            for (int r = 0; r < 32; ++r) {
+                const uint32_t word = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+                const int64_t row = row0 + r;
+                if (row < p.M) {
+                    if (col < p.N) C16[row * p.scm + col] = uint16_t(word & 0xffffu);
+                    if (col + 1 < p.N) C16[row * p.scm + col + 1] = uint16_t(word >> 16);
+                }
             }
         }
     }
@@ -547,10 +628,16 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
             tc_fence_after();
             const int64_t row0 = int64_t(tm) * BM + q * 32;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * BN;
-            epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane, [&] {
+            auto release = [&] {
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));  // accumulator may be overwritten
-            }, 0, epilogue_pace_ns(num_kb, p.cross_tile));
+            };
+            if (p.out_dtype == 0)
+                epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane, release,
+                                         0, epilogue_pace_ns(num_kb, p.cross_tile));
+            else
+                epilogue_tile16<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane,
+                                           release, epilogue_pace_ns(num_kb, p.cross_tile));
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();
@@ -593,11 +680,13 @@ __global__ void tile_map_kernel(Sched s, int32_t num_tiles, int32_t *out) {
 // Split-K reduction: C[i][j] = sum over s = 0 .. S-1, in that order, of
 // W[s][i][j] (W dense [S][M][ldw] fp32). Fixed order: the result does not
 // depend on scheduling. Four consecutive columns per thread.
-__global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restrict__ C, int64_t M,
-                                     int64_t N, int64_t ldw, int64_t scm, int32_t S) {
+__global__ void splitk_reduce_kernel(const float *__restrict__ W, void *__restrict__ Cv, int64_t M,
+                                     int64_t N, int64_t ldw, int64_t scm, int32_t S,
+                                     uint32_t out_dtype, float alpha) {
     const int64_t nq = (N + 3) / 4;
     const int64_t total = M * nq;
     const int64_t slice = M * ldw;
+    float *C = static_cast<float *>(Cv);
     const bool vec_c = (scm % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
@@ -610,6 +699,22 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restr
             acc.y += v.y;
             acc.z += v.z;
             acc.w += v.w;
+        }
+        if (alpha != 1.0f) {
+            acc.x *= alpha;
+            acc.y *= alpha;
+            acc.z *= alpha;
+            acc.w *= alpha;
+        }
+        if (out_dtype != 0) {
+            uint16_t *c16 = static_cast<uint16_t *>(Cv) + i * scm + j;
+            const uint32_t w01 = pack_16x2(acc.x, acc.y, out_dtype);
+            const uint32_t w23 = pack_16x2(acc.z, acc.w, out_dtype);
+            c16[0] = uint16_t(w01 & 0xffffu);
+            if (j + 1 < N) c16[1] = uint16_t(w01 >> 16);
+            if (j + 2 < N) c16[2] = uint16_t(w23 & 0xffffu);
+            if (j + 3 < N) c16[3] = uint16_t(w23 >> 16);
+            continue;
         }
         float *c = C + i * scm + j;
         if (vec_c && j + 3 < N) {
@@ -624,12 +729,15 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, float *__restr
 }
 
 // K == 0: C := 0 (the accumulator starts at zero and no K step adds to it).
-__global__ void zero_c_kernel(float *C, int64_t M, int64_t N, int64_t scm) {
+__global__ void zero_c_kernel(void *C, int64_t M, int64_t N, int64_t scm, int32_t esize) {
     const int64_t total = M * N;
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e - i * N;
-        C[i * scm + j] = 0.0f;
+        if (esize == 4)
+            static_cast<float *>(C)[i * scm + j] = 0.0f;
+        else
+            static_cast<uint16_t *>(C)[i * scm + j] = 0;
     }
 }
 

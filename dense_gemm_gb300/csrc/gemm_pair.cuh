@@ -245,14 +245,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
             tc_fence_after();
             const int64_t row0 = int64_t(tm) * pair::TILE_M + int64_t(rank) * pair::CTA_M + q * 32;
             const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + acc * pair::TILE_N;
-            epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * pair::TILE_N, p, &tmC, stg, buf, lane, [&] {
+            auto release = [&] {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(tdone_bar(acc));
                     mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
                 }
-            }, split, pace);
+            };
+            if (p.out_dtype == 0 || p.splits > 1)  // split-K partials are fp32
+                epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * pair::TILE_N, p, &tmC, stg, buf, lane,
+                                         release, split, pace);
+            else
+                epilogue_tile16<kTmaStore>(t_row, row0, int64_t(tn) * pair::TILE_N, p, &tmC, stg, buf,
+                                           lane, release, pace);
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -104,6 +104,34 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C,
                        int32_t group_size_m, uint32_t schedule_flags,
                        gemm_stream_t stream);
 
+/* Element type of C for gemm_f16_out. */
+#define GEMM_OUT_F32 0
+#define GEMM_OUT_F16 1
+#define GEMM_OUT_BF16 2
+
+/*
+ * gemm_f16_out — C = alpha * (A @ B) stored as fp32, fp16 or bf16.
+ *
+ * The pages keep the product in an FP32 accumulator and store it ([persistent]
+ * "naive tiled matmul"); their C type is never stated. This entry point adds a
+ * scale and 16-bit output: every element is the fp32 accumulator times alpha
+ * (an fp32 multiply, skipped when alpha == 1), rounded to nearest-even into
+ * c_dtype (GEMM_OUT_*; unknown values -> GEMM_ERR_INVALID_ARG). Halving the
+ * output bytes matters when K is small and the store dominates the traffic.
+ * C: device pointer to M x N elements of c_dtype, stride_cn == 1; TMA stores
+ * need a 16-byte-aligned base and stride_cm a multiple of 16 bytes, otherwise
+ * the predicated store path is used. K == 0 writes +0. All other arguments,
+ * layouts and errors as gemm_f16; gemm_f16 equals gemm_f16_out with
+ * GEMM_OUT_F32 and alpha = 1.
+ */
+gemm_status_t gemm_f16_out(const void *A, const void *B, void *C, int32_t c_dtype, float alpha,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t stride_am, int64_t stride_ak,
+                           int64_t stride_bk, int64_t stride_bn,
+                           int64_t stride_cm, int64_t stride_cn,
+                           int32_t group_size_m, uint32_t schedule_flags,
+                           gemm_stream_t stream);
+
 /*
  * gemm_f16_splitk — C = A @ B with the K dimension split across CTA pairs
  * (for problems with fewer output tiles than CTA pairs, e.g. small M x N with

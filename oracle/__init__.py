@@ -17,8 +17,9 @@ Contents
     Row-major and grouped ("CTA swizzle") tile maps, "(2/n) Triton matmul 커널
     탐험 - grouped ordering(CTA swizzle)...", section "구현"; persistent
     visiting order from "(1/n) ...", section "naive persistent matmul".
-``fp16_to_f64``
-    IEEE binary16 decoding from the format definition.
+``fp16_to_f64`` / ``bf16_to_f64`` / ``f64_to_f16_bits`` / ``f64_to_bf16_bits``
+    decoding and round-to-nearest-even encoding of binary16 and bfloat16 from
+    the formats' definitions (for the 16-bit C outputs).
 ``counts``
     FLOP / HBM-byte / panel-size formulas of "4주차 정리: Roofline과 Tiling"
     (sections 1, 2 and 5) and of the "(2/n)" page's section "재사용 거리와 캐시
@@ -58,6 +59,12 @@ def _load():
     lib.oracle_schedule.argtypes = [i64, i64, i64, ctypes.c_int, i64, p]
     lib.oracle_schedule.restype = ctypes.c_int
     lib.oracle_max_threads.restype = ctypes.c_int
+    lib.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_f16.restype = ctypes.c_uint16
+    lib.oracle_f64_to_bf16.argtypes = [ctypes.c_double]
+    lib.oracle_f64_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f64.restype = ctypes.c_double
     lib.oracle_init()
     _lib = lib
     return lib
@@ -70,6 +77,36 @@ def max_threads() -> int:
 
 def fp16_to_f64(bits: int) -> float:
     return float(_load().oracle_fp16_to_f64(int(bits) & 0xFFFF))
+
+
+def f64_to_f16_bits(x: float) -> int:
+    """Nearest binary16 (ties to even) as a bit pattern."""
+    return int(_load().oracle_f64_to_f16(float(x)))
+
+
+def f64_to_bf16_bits(x: float) -> int:
+    """Nearest bfloat16 (ties to even) as a bit pattern."""
+    return int(_load().oracle_f64_to_bf16(float(x)))
+
+
+def bf16_to_f64(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f64(int(bits) & 0xFFFF))
+
+
+def round_output(C64: np.ndarray, dtype: str, alpha: float = 1.0) -> np.ndarray:
+    """round_dtype(alpha * C) elementwise, returned as float64 values.
+
+    dtype: "f32" (IEEE binary32 via numpy's float32 cast, nearest-even),
+    "f16" or "bf16" (this module's rounding)."""
+    x = np.asarray(C64, dtype=np.float64) * alpha
+    if dtype == "f32":
+        return x.astype(np.float32).astype(np.float64)
+    lib = _load()
+    enc = lib.oracle_f64_to_f16 if dtype == "f16" else lib.oracle_f64_to_bf16
+    dec = lib.oracle_fp16_to_f64 if dtype == "f16" else lib.oracle_bf16_to_f64
+    flat = x.ravel()
+    out = np.fromiter((dec(enc(float(v))) for v in flat), dtype=np.float64, count=flat.size)
+    return out.reshape(x.shape)
 
 
 def _as_f16(x):

@@ -61,6 +61,65 @@ double oracle_fp16_to_f64(uint16_t h) {
     return s ? -v : v;
 }
 
+/* ---------------------------------------------------------------------------
+ * Rounding to a 16-bit IEEE-style format, from the formats' definitions:
+ * sign bit, `ebits` exponent bits with bias 2^(ebits-1) - 1, `mbits` fraction
+ * bits; binary16 is (5, 10), bfloat16 is (8, 7). Round to nearest, ties to the
+ * even fraction (nearbyint in the default rounding mode); values at or beyond
+ * the midpoint between the largest finite value and 2^(emax+1) become
+ * infinity; NaN -> quiet NaN. Returns the bit pattern.
+ * ------------------------------------------------------------------------- */
+static uint16_t round_ieee16(double x, int ebits, int mbits) {
+    const int bias = (1 << (ebits - 1)) - 1;
+    const int emax = bias, emin = 1 - bias;
+    const uint16_t sign = signbit(x) ? (uint16_t)(1u << 15) : 0;
+    const uint16_t inf = (uint16_t)(((1u << ebits) - 1u) << mbits);
+    if (isnan(x)) return (uint16_t)(inf | (1u << (mbits - 1)));
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    /* largest finite: (2 - 2^-mbits) * 2^emax; overflow from the midpoint up */
+    const double limit = ldexp(2.0 - ldexp(1.0, -(mbits + 1)), emax);
+    if (a >= limit) return (uint16_t)(sign | inf);
+    int e2;
+    frexp(a, &e2);          /* a = f * 2^e2, f in [0.5, 1): a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;
+    if (E < emin) E = emin; /* subnormal range shares the smallest normal's quantum */
+    const double q = ldexp(1.0, E - mbits);
+    double n = nearbyint(a / q); /* exact scaling by a power of two, then RNE */
+    /* n in [0, 2^(mbits+1)]; 2^(mbits+1) carries into the next binade */
+    uint32_t bits;
+    if (E == emin && n < ldexp(1.0, mbits)) {
+        bits = (uint32_t)n; /* subnormal (or the smallest normal when n reaches 2^mbits) */
+    } else {
+        if (n >= ldexp(1.0, mbits + 1)) {
+            n = ldexp(1.0, mbits);
+            E += 1;
+        }
+        if (E > emax) return (uint16_t)(sign | inf);
+        bits = ((uint32_t)(E + bias) << mbits) | (uint32_t)(n - ldexp(1.0, mbits));
+    }
+    return (uint16_t)(sign | bits);
+}
+
+uint16_t oracle_f64_to_f16(double x) { return round_ieee16(x, 5, 10); }
+uint16_t oracle_f64_to_bf16(double x) { return round_ieee16(x, 8, 7); }
+
+/* bfloat16 -> double from the format (8 exponent bits, bias 127, 7 fraction bits). */
+double oracle_bf16_to_f64(uint16_t h) {
+    int s = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -133); /* 2^-126 * f / 2^7 */
+    } else if (e == 255) {
+        v = (f == 0) ? INFINITY : NAN;
+    } else {
+        v = ldexp(128.0 + (double)f, e - 134); /* 2^(e-127) * (128+f) / 2^7 */
+    }
+    return s ? -v : v;
+}
+
 /* Decode table: one entry per 16-bit pattern, filled from the function above. */
 static double g_h2d[65536];
 static int g_h2d_ready = 0;

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert "gemm_f16" in names and "gemm_f16_tile_map" in names
-    assert len(names) == 11, names
+    assert len(names) == 12, names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -145,3 +145,12 @@ def test_splitk_host_validation(lib):
     args = [a[k] for k in ("A", "B", "C", "M", "N", "K", "sam", "sak", "sbk", "sbn", "scm", "scn")]
     assert lib.gemm_f16_splitk(*args, -1, None, 0, 8, 3, None) == 1
     assert lib.gemm_f16_splitk(*args[:3], 0, *args[4:], 4, None, 0, 8, 3, None) == 0  # M == 0
+
+
+def test_out_dtype_validation(lib):
+    import ctypes as C
+    args = (16, 16, 16)
+    # unknown element type -> INVALID_ARG before any GPU work
+    assert lib.gemm_f16_out(*args, 3, C.c_float(1.0), 4, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 1
+    assert lib.gemm_f16_out(*args, -1, C.c_float(1.0), 4, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 1
+    assert lib.gemm_f16_out(*args, 1, C.c_float(2.0), 0, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 0

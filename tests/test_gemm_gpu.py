@@ -391,3 +391,72 @@ def test_splitk_rejects_small_workspace_and_unaligned_operands():
     with pytest.raises(GemmError) as e:
         gemm_splitk(A2, B2, splits=2)
     assert e.value.status == 2
+
+
+# ------------------------------------------------------------------ 16-bit C and alpha
+
+OUT_TYPES = [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")]
+
+
+@pytest.mark.parametrize("dtype,name", OUT_TYPES)
+@pytest.mark.parametrize("alpha", [1.0, 0.5, -2.0])
+@pytest.mark.parametrize("shape,single", [((300, 600, 200), False), ((512, 512, 4096), False),
+                                          ((129, 257, 65), True), ((640, 384, 1000), False)])
+def test_out_dtype_alpha_integer_bit_exact(dtype, name, alpha, shape, single):
+    # integer inputs: the fp32 accumulator and alpha * acc are exact (alpha a power
+    # of two), so both sides round the same value to the output type
+    M, N, K = shape
+    A = draw(M, K, "int", 400 + M)
+    B = draw(K, N, "int", 401 + N)
+    want = oracle.round_output(oracle.gemm(A, B), name, alpha)
+    C = gemm(to_dev(A), to_dev(B), out_dtype=dtype, alpha=alpha, single_cta=single)
+    torch.cuda.synchronize()
+    assert C.dtype == dtype
+    assert np.array_equal(C.double().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("dtype,name,ulp", [(torch.float16, "f16", 2.0 ** -10),
+                                            (torch.bfloat16, "bf16", 2.0 ** -7)])
+def test_out_dtype_random_within_bound(dtype, name, ulp):
+    M, N, K = 1000, 1200, 1500
+    A = draw(M, K, "normal", 420)
+    B = relayout(draw(K, N, "normal", 421), "col")
+    exact = oracle.gemm(A, B)
+    alpha = 0.75
+    C = gemm(to_dev(A), to_dev(B), out_dtype=dtype, alpha=alpha)
+    torch.cuda.synchronize()
+    got = C.double().cpu().numpy()
+    ref = alpha * exact
+    # stated bound (scaled by |alpha|) plus one unit in the last place of the output type
+    from gpu_util import error_bound
+    tol = abs(alpha) * error_bound(A, B) + ulp * np.abs(ref)
+    assert np.all(np.abs(got - ref) <= tol)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-3 + ulp
+
+
+@pytest.mark.parametrize("dtype,name", OUT_TYPES[1:])
+def test_out_dtype_predicated_store_and_k0(dtype, name):
+    M, N, K = 257, 301, 130
+    A = draw(M, K, "int", 430)
+    B = draw(K, N, "int", 431)
+    want = oracle.round_output(oracle.gemm(A, B), name, 1.0)
+    buf = torch.full((M * 311 + 3,), float("nan"), dtype=dtype, device="cuda")
+    C = buf.as_strided((M, N), (311, 1), 3)  # odd stride, misaligned base: predicated stores
+    gemm(to_dev(A), to_dev(B), C)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.double().cpu().numpy(), want)
+    Z = torch.full((M, N), 3.0, dtype=dtype, device="cuda")
+    gemm(torch.zeros(M, 0, dtype=torch.float16, device="cuda"),
+         torch.zeros(0, N, dtype=torch.float16, device="cuda"), Z)
+    torch.cuda.synchronize()
+    assert (Z == 0).all()
+
+
+def test_out_dtype_split_k_applies_alpha_once():
+    from dense_gemm_gb300 import gemm_splitk
+    A = draw(512, 2048, "int", 440)
+    B = draw(2048, 512, "int", 441)
+    exact = oracle.gemm(A, B)
+    C = gemm_splitk(to_dev(A), to_dev(B), splits=4)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), exact)

@@ -308,3 +308,84 @@ def test_random_shapes_schedule_consistency():
         nm, nn, G, grid = rng.randint(1, 60), rng.randint(1, 60), rng.randint(1, 16), rng.randint(1, 200)
         s = oracle.schedule(nm, nn, G, True, grid)
         assert _check_bijection(s, nm, nn)
+
+
+# ------------------------------------------------ 16-bit output rounding (C as fp16 / bf16)
+
+def _special_values():
+    vals = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 1e6, 2.0 ** -24, 2.0 ** -25,
+            3 * 2.0 ** -26, 2.0 ** -14, 2.0 ** -14 - 2.0 ** -25, 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11,
+            3.0e38, 3.4e38, 2.0 ** -126, 2.0 ** -133, 2.0 ** -134, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8]
+    return vals + [-v for v in vals]
+
+
+def test_bf16_decode_exhaustive_vs_torch():
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    ref = bits.view(torch.bfloat16).double().numpy()
+    ours = np.array([oracle.bf16_to_f64(int(b) & 0xFFFF) for b in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_f16_rounding_matches_numpy():
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000),
+                         np.array(_special_values())])
+    # exact ties: midpoints between neighbouring binary16 values
+    b = rng.integers(0, 0x7BFF, 3000).astype(np.uint16)
+    lo = b.view(np.float16).astype(np.float64)
+    hi = (b + 1).astype(np.uint16).view(np.float16).astype(np.float64)
+    xs = np.concatenate([xs, (lo + hi) / 2, -(lo + hi) / 2])
+    ref = xs.astype(np.float16).view(np.uint16)
+    ours = np.array([oracle.f64_to_f16_bits(x) for x in xs], dtype=np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "bf16"])
+def test_rounding_is_nearest_ties_to_even_brute_force(fmt):
+    enc = oracle.f64_to_f16_bits if fmt == "f16" else oracle.f64_to_bf16_bits
+    dec = oracle.fp16_to_f64 if fmt == "f16" else oracle.bf16_to_f64
+    top = 0x7BFF if fmt == "f16" else 0x7F7F  # largest finite
+    rng = np.random.default_rng(8)
+    xs = list(rng.standard_normal(3000) * 10.0 ** rng.uniform(-45 if fmt == "bf16" else -9,
+                                                              38 if fmt == "bf16" else 4.8, 3000))
+    xs += [v for v in _special_values() if np.isfinite(v)]
+    for x in xs:
+        r = enc(x)
+        mag = r & 0x7FFF
+        if mag > top:  # infinity: only beyond the last finite value's half-ulp
+            assert abs(x) > dec(top)
+            continue
+        got = abs(dec(r))
+        for nb in (mag - 1, mag + 1):
+            if 0 <= nb <= top:
+                d_nb, d_r = abs(abs(x) - dec(nb)), abs(abs(x) - got)
+                assert d_r <= d_nb, (fmt, x, hex(r), hex(nb))
+                if d_r == d_nb:  # a tie goes to the even fraction
+                    assert mag % 2 == 0, (fmt, x, hex(r))
+        if x != 0:
+            assert (r >> 15) == (1 if x < 0 else 0)
+
+
+def test_rounding_landmarks():
+    f = oracle.f64_to_f16_bits
+    assert f(65504.0) == 0x7BFF and f(65519.99) == 0x7BFF and f(65520.0) == 0x7C00
+    assert f(2.0 ** -24) == 0x0001 and f(2.0 ** -25) == 0x0000 and f(3 * 2.0 ** -26) == 0x0001
+    assert f(1 + 2.0 ** -11) == 0x3C00 and f(1 + 3 * 2.0 ** -11) == 0x3C02
+    assert f(-0.0) == 0x8000 and (f(float("nan")) & 0x7C00) == 0x7C00
+    g = oracle.f64_to_bf16_bits
+    assert g(1.0) == 0x3F80 and g(1 + 2.0 ** -8) == 0x3F80 and g(1 + 3 * 2.0 ** -8) == 0x3F82
+    assert g(2.0 ** -133) == 0x0001 and g(2.0 ** -134) == 0x0000
+    assert g(3.4e38) == 0x7F80  # past the midpoint between 0x7F7F (3.3895e38) and 2^128
+    assert g(3.0e38) == 0x7F62  # 3.0e38 = 1.7633 * 2^127 -> fraction 0x62
+    assert g(-2.0) == 0xC000
+
+
+def test_round_output_alpha_and_formats():
+    C = np.array([[1.0, -3.0], [65519.0, 1e-8]])
+    assert np.array_equal(oracle.round_output(C, "f32", 0.5), np.float32(C * 0.5).astype(np.float64))
+    r16 = oracle.round_output(C, "f16", 2.0)
+    assert r16[0, 0] == 2.0 and r16[0, 1] == -6.0 and np.isinf(r16[1, 0]) and r16[1, 1] == 0.0
+    rb = oracle.round_output(C, "bf16", 1.0)
+    assert rb[0, 0] == 1.0 and rb[1, 0] == 65536.0
