@@ -55,7 +55,7 @@ def parse_args(argv=None):
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
     p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
-                                       "outdtype"],
+                                       "outdtype", "ragged"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
@@ -439,7 +439,9 @@ def run_sweep(args):
     splitk - gemm_f16 vs gemm_f16_splitk (automatic slices) on 512^3 and
              1024^2 x 32768 (fewer tiles than CTA pairs);
     outdtype - fp32 vs fp16 vs bf16 C (gemm_f16_out) on the headline workload
-               and at K = 512, where the C store dominates the traffic."""
+               and at K = 512, where the C store dominates the traffic;
+    ragged - the two ragged workloads (4000 x 5000 x 3000 through TMA, 8191^2 x 257
+             with 514-byte rows through the predicated-load path) and 512^3."""
     import torch
     from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
@@ -451,6 +453,9 @@ def run_sweep(args):
     elif args.sweep == "ksweep":
         names = [n for n in WORKLOADS if n.startswith("ksweep_")]
         points = [dict(grouped=True, cross_tile=c, single_cta=False) for c in (True, False)]
+    elif args.sweep == "ragged":
+        names = ["ragged_4000x5000x3000", "ragged_8191x8191x257", "square_512"]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False)]
     elif args.sweep == "outdtype":
         names = [HEADLINE, "ksweep_16384x16384x512"]
         points = [("out", torch.float32), ("out", torch.float16), ("out", torch.bfloat16)]
