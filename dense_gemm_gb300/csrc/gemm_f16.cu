@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <numeric>
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
@@ -50,7 +51,7 @@ bool log_enabled() {
 template <bool L, bool S>
 cudaError_t set_smem_attr() {
     return cudaFuncSetAttribute(gemm_f16_persistent<L, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                SMEM_BYTES);
+                                Layout<L>::smem_bytes);
 }
 
 template <bool S>
@@ -112,7 +113,8 @@ EncodeTiledFn encode_fn() {
 
 // 2-D tiled tensor map, inner dimension first, 128-byte swizzle, OOB -> zero.
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, uint64_t inner,
-               uint64_t outer, uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t outer, uint64_t outer_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {inner, outer};
@@ -120,8 +122,37 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Alignment classes of one operand for the predicated-load kernel: `rows` rows
+// of `cols` contiguous fp16 elements, row rho starting at X + 2*S*rho bytes.
+// Rows with rho mod P == c share their offset m_c inside a 16-byte granule and
+// are 2*S*P bytes apart (a multiple of 16), so class c is one tensor map whose
+// rows start m_c bytes early, at the granule boundary, and whose width grows by
+// m_c/2 elements. Every byte TMA reads through these maps therefore shares its
+// granule with an element of the operand. Returns false if a map is rejected.
+bool encode_classes(CUtensorMap *maps, const void *X, int64_t S, int64_t rows, int64_t cols,
+                    uint32_t *P_out, uint32_t *mis, uint32_t *live) {
+    const uint64_t r = (2u * uint64_t(S)) % 16u;
+    const uint64_t P = r == 0 ? 1u : 16u / std::gcd(r, uint64_t(16));
+    *P_out = uint32_t(P);
+    *mis = 0;
+    *live = 0;
+    for (uint64_t c = 0; c < P; ++c) {
+        if (uint64_t(rows) <= c) continue;  // no row in this class: its lines are placed as zeros
+        const uint64_t nrows = (uint64_t(rows) - c + P - 1) / P;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(X) + 2u * uint64_t(S) * c;
+        const uint32_t m = uint32_t(a & 15u);
+        if (!encode_2d(&maps[c], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, reinterpret_cast<const void *>(a - m),
+                       uint64_t(cols) + m / 2u, nrows, 2u * uint64_t(S) * P, BOX_W, BOX_H,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
+        *mis |= m << (4u * c);
+        *live |= 1u << c;
+    }
+    return true;
 }
 
 // 3-D tiled tensor map (inner first) with a box of depth 1 in the outermost
@@ -153,8 +184,12 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <bool L, bool S>
 cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
-                   int grid, cudaStream_t stream) {
-    gemm_f16_persistent<L, S><<<grid, cta_threads(L), SMEM_BYTES, stream>>>(a, b, c, p);
+                   const ClassMaps &cm, int grid, cudaStream_t stream) {
+    if constexpr (L)
+        gemm_f16_persistent<L, S><<<grid, cta_threads(L), Layout<L>::smem_bytes, stream>>>(a, b, c, p,
+                                                                                           NoClassMaps{});
+    else
+        gemm_f16_persistent<L, S><<<grid, cta_threads(L), Layout<L>::smem_bytes, stream>>>(a, b, c, p, cm);
     return cudaGetLastError();
 }
 
@@ -306,6 +341,17 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                          MN_CHUNK, BK);
         if (!okA || !okB) return GEMM_ERR_CUDA;
     }
+    static_assert(sizeof(ClassMaps) == 2 * MAX_CLASSES * sizeof(CUtensorMap), "");
+    ClassMaps cm;
+    std::memset(&cm, 0, sizeof(cm));
+    uint32_t cls_p[2] = {1, 1}, cls_mis[2] = {0, 0}, cls_live[2] = {0, 0};
+    if (!load_tma) {
+        const bool okA = a_k ? encode_classes(cm.a, A, stride_am, M, K, &cls_p[0], &cls_mis[0], &cls_live[0])
+                             : encode_classes(cm.a, A, stride_ak, K, M, &cls_p[0], &cls_mis[0], &cls_live[0]);
+        const bool okB = b_n ? encode_classes(cm.b, B, stride_bk, K, N, &cls_p[1], &cls_mis[1], &cls_live[1])
+                             : encode_classes(cm.b, B, stride_bn, N, K, &cls_p[1], &cls_mis[1], &cls_live[1]);
+        if (!okA || !okB) return GEMM_ERR_UNSUPPORTED;
+    }
     SplitPlan sp{1, int32_t(cdiv(K, BK)), N};
     if (sk.enabled) {
         sp = plan_splits(M, N, K, sk.splits, ds->max_pairs);
@@ -357,6 +403,11 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     p.b_mn = b_n ? 1u : 0u;
     p.idesc = make_idesc(p.a_mn, p.b_mn, use_pair ? 2 * pair::CTA_M : BM, tile_n);
     p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
+    for (int op = 0; op < 2; ++op) {
+        p.cls_lp[op] = uint32_t(__builtin_ctz(cls_p[op]));
+        p.cls_mis[op] = cls_mis[op];
+        p.cls_live[op] = cls_live[op];
+    }
     if (!use_pair) {  // the one-CTA kernel walks whole tiles
         p.splits = 1;
         p.kb_per_split = p.num_kb;
@@ -400,10 +451,10 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     } else if (use_pair)
         e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
                       : launch_pair<false>(tmA, tmB, tmC, p, grid, stream);
-    else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, grid, stream);
-    else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, grid, stream);
-    else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, grid, stream);
-    else e = launch<false, false>(tmA, tmB, tmC, p, grid, stream);
+    else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
+    else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, cm, grid, stream);
+    else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, cm, grid, stream);
+    else e = launch<false, false>(tmA, tmB, tmC, p, cm, grid, stream);
     return e == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -523,7 +574,9 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *stat
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;
     if (static_smem) *static_smem = int32_t(a.sharedSizeBytes);
-    if (dynamic_smem) *dynamic_smem = variant >= 4 ? pair::SMEM_BYTES : SMEM_BYTES;
+    if (dynamic_smem)
+        *dynamic_smem = variant >= 4 ? pair::SMEM_BYTES
+                        : variant >= 2 ? Layout<false>::smem_bytes : Layout<true>::smem_bytes;
     if (threads) *threads = thr;
     return GEMM_OK;
 }

@@ -54,19 +54,72 @@ constexpr int EPI_COLS = 32;                       // fp32 columns per epilogue 
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;   // 32 rows x 128 B
 constexpr int EPI_BUFS = 2;
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
-constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 * NUM_ACC + 1;
-constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = OFF_TMEM_SLOT + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 B
+// Predicated-load path: for operands that one tensor map cannot describe (a
+// row stride or a base address that is not a multiple of 16 bytes).
+// Terms: a "row" of an operand runs along its unit stride (K for a K-major
+// operand, M or N for an M/N-major one); S is the element distance between
+// rows. A "line" is 64 elements of one row: one 128-byte swizzle row of a
+// stage. Rows rho with rho mod P == c (P = 16 / gcd(2S mod 16, 16) <= 8) form
+// alignment class c: they all start m_c bytes into a 16-byte granule, and two
+// consecutive rows of a class are 2*S*P bytes apart, a multiple of 16. Each
+// class gets its own tensor map whose rows begin at those granule boundaries,
+// so TMA copies boxes of 8 class rows x 72 elements (a line plus up to 7
+// leading elements) into a staging ring, with zero fill past the matrix
+// edges, and the loader warps shift each line by m_c bytes into the stage.
+constexpr int PRED_LOAD_WARPS = 3;
+constexpr int MAX_CLASSES = 8;
+constexpr int BOX_W = 72;                           // elements per staged line
+constexpr int BOX_H = 8;                            // class rows per box
+constexpr int LINE_PITCH = BOX_W * 2;               // 144 bytes
+constexpr int BOX_BYTES = BOX_H * LINE_PITCH;       // 1152 = 9 x 128
+constexpr int GROUP_BOXES = 8;                      // 64 lines per copy group
+constexpr int GROUP_BYTES = GROUP_BOXES * BOX_BYTES;
+constexpr int COPY_DEPTH = 3;                       // copy groups in flight per loader warp
+constexpr int A_GROUPS = BM / 64, B_GROUPS = BN / 64;
+constexpr int GROUPS_PER_KB = A_GROUPS + B_GROUPS;  // 6
+constexpr int WARP_GROUPS = GROUPS_PER_KB / PRED_LOAD_WARPS;  // per loader warp and K-block
+static_assert(GROUPS_PER_KB % PRED_LOAD_WARPS == 0, "equal loader shares");
 
-static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0, "swizzled buffers need 1 KiB alignment");
-static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+// Shared-memory map of the one-CTA kernel. The predicated-load variant keeps
+// two operand stages and holds the loader warps' staging rings (with one
+// mbarrier per ring slot) in the space of the others.
+template <bool kTmaLoad>
+struct Layout {
+    static constexpr int stages = kTmaLoad ? STAGES : 2;
+    static constexpr int off_a = 0;
+    static constexpr int off_b = off_a + stages * A_STAGE_BYTES;
+    static constexpr int off_epi = off_b + stages * B_STAGE_BYTES;
+    static constexpr int off_copy = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+    static constexpr int copy_slots = kTmaLoad ? 0 : PRED_LOAD_WARPS * COPY_DEPTH;
+    static constexpr int off_bar = off_copy + copy_slots * GROUP_BYTES;
+    static constexpr int copy_bar0 = 2 * stages + 2 * NUM_ACC + 1;  // index of the first slot barrier
+    static constexpr int num_bars = copy_bar0 + copy_slots;
+    static constexpr int off_tmem_slot = off_bar + num_bars * 8;
+    static constexpr int smem_bytes = off_tmem_slot + 16 + 1024;  // slack to align the base to 1 KiB
+    static_assert(off_b % 1024 == 0 && off_epi % 1024 == 0, "swizzled buffers need 1 KiB alignment");
+    static_assert(off_copy % 128 == 0 && GROUP_BYTES % 128 == 0 && BOX_BYTES % 128 == 0,
+                  "TMA box destinations need 128-byte alignment");
+    static_assert(smem_bytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+};
 
-__host__ __device__ constexpr int load_warps(bool tma_load) { return tma_load ? 1 : 4; }
+// Tensor maps of the alignment classes of A and B (predicated-load variant).
+struct ClassMaps {
+    CUtensorMap a[MAX_CLASSES];
+    CUtensorMap b[MAX_CLASSES];
+};
+struct NoClassMaps {
+    uint32_t unused;
+};
+template <bool kTmaLoad>
+struct ClassMapsFor {
+    using type = ClassMaps;
+};
+template <>
+struct ClassMapsFor<true> {
+    using type = NoClassMaps;
+};
+
+__host__ __device__ constexpr int load_warps(bool tma_load) { return tma_load ? 1 : PRED_LOAD_WARPS; }
 __host__ __device__ constexpr int cta_threads(bool tma_load) {
     return (load_warps(tma_load) + 1 + EPI_WARPS) * 32;
 }
@@ -190,6 +243,12 @@ struct Params {
     uint32_t cross_tile;
     uint32_t l2_mode;   // bit 0: C stores evict-first; bit 1: A/B loads evict-last (pair kernel)
     uint32_t out_dtype; // C element type: 0 fp32, 1 fp16, 2 bf16 (nearest-even)
+    // predicated loads, per operand (0 = A, 1 = B): log2 of the class count P,
+    // each class's byte offset in its first granule (4 bits per class), and
+    // the classes that hold rows
+    uint32_t cls_lp[2];
+    uint32_t cls_mis[2];
+    uint32_t cls_live[2];
     float alpha;        // C = alpha * (A @ B)
     WaitCtl wait;
 };
@@ -248,40 +307,150 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
     return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
-// Predicated copy of one operand tile into the swizzled layout the descriptors
-// above describe; elements outside [0, mn_ext) x [0, K) read as zero.
-// X(mn, k) = X[mn * s_mn + k * s_k].
-template <int R>
-__device__ __forceinline__ void load_operand_tile(uint32_t dst, const uint16_t *X, int64_t mn0,
-                                                  int64_t mn_ext, int64_t k0, int64_t K,
-                                                  int64_t s_mn, int64_t s_k, uint32_t mn_major,
-                                                  int tid, int nthreads) {
-    constexpr int CHUNKS = R * BK / 8;  // 8 contiguous elements per chunk
-    for (int c = tid; c < CHUNKS; c += nthreads) {
-        uint32_t off;
-        int64_t mn, k;
-        if (!mn_major) {  // chunk = 8 consecutive k of one mn
-            const int r = c >> 3, u = c & 7;
-            off = swz128(r, u);
-            mn = mn0 + r;
-            k = k0 + u * 8;
-        } else {  // chunk = 8 consecutive mn of one k
-            const int kk = c / (R / 8), mc = c % (R / 8);
-            off = uint32_t(mc >> 3) * MN_CHUNK_BYTES + swz128(kk, mc & 7);
-            mn = mn0 + mc * 8;
-            k = k0 + kk;
+// ------------------------------------------------------------------ predicated loads
+// Position of a predicated loader warp in the static work sequence: tile
+// (it-th of this CTA), K-block, and which of the warp's copy groups of that
+// K-block (group index warp + PRED_LOAD_WARPS * g of GROUPS_PER_KB).
+struct LineCursor {
+    int32_t tile, it, kb, g;
+    int64_t m0, n0;
+
+    __device__ __forceinline__ void coords(const Params &p) {
+        if (tile < p.num_tiles) {
+            int32_t tm, tn;
+            tile_coords(tile, p.sched, tm, tn);
+            m0 = int64_t(tm) * BM;
+            n0 = int64_t(tn) * BN;
         }
-        uint32_t w[4];
+    }
+    __device__ __forceinline__ void start(int32_t first, const Params &p) {
+        tile = first;
+        it = kb = g = 0;
+        m0 = n0 = 0;
+        coords(p);
+    }
+    __device__ __forceinline__ bool valid(const Params &p) const { return tile < p.num_tiles; }
+    __device__ __forceinline__ void next(const Params &p, int32_t grid) {
+        if (++g < WARP_GROUPS) return;
+        g = 0;
+        if (++kb < p.num_kb) return;
+        kb = 0;
+        tile += grid;
+        ++it;
+        coords(p);
+    }
+};
+
+// Copy group `gamma` (0 .. GROUPS_PER_KB-1) of a K-block: the first A_GROUPS
+// groups hold A's 128 lines, the rest B's 256, 64 lines (8 boxes) each. Box
+// beta of an operand covers class c, row block b (8 class rows) and 64-element
+// segment s, with s fastest: an operand has NS = R/64 segments per row when
+// M/N-major (rows are k) and 1 when K-major (rows are m or n).
+struct GroupShape {
+    int op;              // 0 = A, 1 = B
+    int first_box;       // beta of the group's first box
+    int lp, lns, lbc;    // log2 of: classes P, segments per row NS, row blocks per class
+    uint32_t mn_major;
+    int64_t mn0;
+
+    // box beta -> class, row block, segment (all counts are powers of two)
+    __device__ __forceinline__ int cls(int beta) const { return beta >> (lbc + lns); }
+    __device__ __forceinline__ int blk(int beta) const { return (beta >> lns) & ((1 << lbc) - 1); }
+    __device__ __forceinline__ int seg(int beta) const { return beta & ((1 << lns) - 1); }
+};
+
+__device__ __forceinline__ GroupShape group_shape(const Params &p, int gamma, int64_t m0, int64_t n0) {
+    GroupShape gs;
+    const bool is_a = gamma < A_GROUPS;
+    gs.op = is_a ? 0 : 1;
+    gs.first_box = (is_a ? gamma : gamma - A_GROUPS) * GROUP_BOXES;
+    gs.mn_major = is_a ? p.a_mn : p.b_mn;
+    gs.lp = int(is_a ? p.cls_lp[0] : p.cls_lp[1]);
+    // R = 128 (A) or 256 (B) lines: NS = R/64 when M/N-major, else 1; rows per
+    // operand tile NR = 64 (k) when M/N-major, else R; Bc = NR / (8 P)
+    const int lr = is_a ? 7 : 8;
+    gs.lns = gs.mn_major ? lr - 6 : 0;
+    gs.lbc = (gs.mn_major ? 6 : lr) - 3 - gs.lp;
+    gs.mn0 = is_a ? m0 : n0;
+    return gs;
+}
+
+// Starts the TMA copies of one group into ring slot `slot`; they complete on
+// `bar`. Lane 0 announces the byte count, then lane i < 8 issues box i (boxes
+// of classes without rows are skipped and placed as zeros). Whole warp.
+__device__ __forceinline__ void issue_class_group(const Params &p, const ClassMaps &cm,
+                                                  const LineCursor &c, int gamma, uint32_t slot,
+                                                  uint32_t bar, int lane) {
+    const GroupShape gs = group_shape(p, gamma, c.m0, c.n0);
+    const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
+    if (lane == 0) {
+        uint32_t boxes = 0;
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-            uint32_t lo = 0, hi = 0;
-            const int64_t mn_a = mn_major ? mn + e : mn, k_a = mn_major ? k : k + e;
-            const int64_t mn_b = mn_major ? mn + e + 1 : mn, k_b = mn_major ? k : k + e + 1;
-            if (mn_a < mn_ext && k_a < K) lo = __ldg(X + mn_a * s_mn + k_a * s_k);
-            if (mn_b < mn_ext && k_b < K) hi = __ldg(X + mn_b * s_mn + k_b * s_k);
-            w[e >> 1] = lo | (hi << 16);
+        for (int i = 0; i < GROUP_BOXES; ++i) boxes += (live >> gs.cls(gs.first_box + i)) & 1u;
+        fence_proxy_async_smem();  // this slot's staging reads precede the new copies
+        mbar_arrive_expect_tx(bar, boxes * BOX_BYTES);
+    }
+    __syncwarp();
+    if (lane < GROUP_BOXES) {
+        const int64_t k0 = int64_t(c.kb) * BK;
+        const int32_t xb = int32_t(gs.mn_major ? gs.mn0 : k0);              // unit-stride coordinate
+        const int32_t yb = int32_t((gs.mn_major ? k0 : gs.mn0) >> gs.lp);  // class row of the tile's first row
+        const int beta = gs.first_box + lane, cls = gs.cls(beta);
+        const CUtensorMap *maps = gs.op == 0 ? cm.a : cm.b;
+        if ((live >> cls) & 1u)
+            tma_load_2d(slot + uint32_t(lane) * BOX_BYTES, &maps[cls], xb + 64 * gs.seg(beta),
+                        yb + BOX_H * gs.blk(beta), bar);
+    }
+}
+
+// Bytes [m, m + 16) of the 32-byte window w[0..7] (m even, 0..14): select
+// by whole words (m / 4), then shift by a half word when m % 4 == 2.
+__device__ __forceinline__ void window16(const uint32_t (&w)[8], uint32_t m, uint32_t (&o)[4]) {
+    uint32_t x[6], y[5];
+#pragma unroll
+    for (int t = 0; t < 6; ++t) x[t] = (m & 8u) ? w[t + 2] : w[t];
+#pragma unroll
+    for (int t = 0; t < 5; ++t) y[t] = (m & 4u) ? x[t + 1] : x[t];
+    const uint32_t sel = (m & 2u) ? 0x5432u : 0x3210u;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) o[t] = __byte_perm(y[t], y[t + 1], sel);
+}
+
+// All lanes: shift the group's 64 staged lines (8 boxes of 8) into the operand
+// stage at `dst`. In step j of a pair of boxes, lane l moves 16 bytes: unit
+// l % 8 of line 4j + l / 8; each box has one class and thus one offset m.
+__device__ __forceinline__ void place_class_group(const Params &p, const GroupShape &gs, uint32_t slot,
+                                                  uint32_t dst, int lane) {
+    const uint32_t mis = gs.op == 0 ? p.cls_mis[0] : p.cls_mis[1];
+    const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
+    const uint32_t u = uint32_t(lane) & 7u, r4 = uint32_t(lane) >> 3;
+    const uint32_t seg_bytes = gs.mn_major ? uint32_t(MN_CHUNK_BYTES) : 0u;
+#pragma unroll 1
+    for (int bx = 0; bx < GROUP_BOXES; bx += 2) {
+        uint32_t w[4][8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // the staging reads of both boxes first
+            const uint32_t src = slot + (uint32_t(8 * bx + 4 * j) + r4) * LINE_PITCH + 16u * u;
+            ld_shared_v4(src, w[j][0], w[j][1], w[j][2], w[j][3]);
+            ld_shared_v4(src + 16u, w[j][4], w[j][5], w[j][6], w[j][7]);
         }
-        st_shared_v4(dst + off, w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int beta = gs.first_box + bx + h, cls = gs.cls(beta);
+            const uint32_t m = (mis >> (4 * cls)) & 15u;  // where the lines start in their window
+            const bool has_rows = (live >> cls) & 1u;
+            const uint32_t row0 = uint32_t(BOX_H * gs.blk(beta));
+            const uint32_t seg_off = uint32_t(gs.seg(beta)) * seg_bytes;
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * h + jj;
+                uint32_t o[4];
+                window16(w[j], m, o);
+                if (!has_rows) o[0] = o[1] = o[2] = o[3] = 0u;
+                const uint32_t rho = uint32_t(cls) + ((row0 + 4u * uint32_t(jj) + r4) << gs.lp);
+                st_shared_v4(dst + seg_off + rho * 128u + ((u ^ (rho & 7u)) << 4), o[0], o[1], o[2], o[3]);
+            }
+        }
     }
 }
 
@@ -351,12 +520,15 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
             for (int u = 0; u < 8; ++u)
                 st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
             __syncwarp();
-            const int64_t col = col0 + lane;
-#pragma unroll 4
-            for (int r = 0; r < 32; ++r) {
-                const uint32_t bits = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
-                const int64_t row = row0 + r;
-                if (row < p.M && col < p.N) p.C[row * p.scm + col] = __uint_as_float(bits);
+            // all 32 staging reads first, so that no read waits behind a store
+#pragma unroll
+            for (int r = 0; r < 32; ++r) v[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+            const int64_t col = col0 + lane, rows = p.M - row0;
+            if (col < p.N) {
+                float *dst = p.C + row0 * p.scm + col;
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    if (r < rows) dst[r * p.scm] = __uint_as_float(v[r]);
             }
         }
     }
@@ -421,15 +593,18 @@ __device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, in
             for (int u = 0; u < 8; ++u)
                 st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             __syncwarp();
-            const int64_t col = col0 + 2 * lane;  // this lane: columns col, col + 1
-            uint16_t *C16 = reinterpret_cast<uint16_t *>(p.C);
-#pragma unroll 4
-            for (int r = 0; r < 32; ++r) {
-                const uint32_t word = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
-                const int64_t row = row0 + r;
-                if (row < p.M) {
-                    if (col < p.N) C16[row * p.scm + col] = uint16_t(word & 0xffffu);
-                    if (col + 1 < p.N) C16[row * p.scm + col + 1] = uint16_t(word >> 16);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) w[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+            const int64_t col = col0 + 2 * lane, rows = p.M - row0;  // this lane: columns col, col + 1
+            if (col < p.N) {
+                uint16_t *dst = reinterpret_cast<uint16_t *>(p.C) + row0 * p.scm + col;
+                const bool both = col + 1 < p.N;
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    if (r < rows) {
+                        dst[r * p.scm] = uint16_t(w[r] & 0xffffu);
+                        if (both) dst[r * p.scm + 1] = uint16_t(w[r] >> 16);
+                    }
                 }
             }
         }
@@ -441,31 +616,34 @@ template <bool kTmaLoad, bool kTmaStore>
 __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
     gemm_f16_persistent(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const Params p) {
+                        const __grid_constant__ CUtensorMap tmC, const Params p,
+                        const __grid_constant__ typename ClassMapsFor<kTmaLoad>::type cm) {
     constexpr int LOAD_WARPS = load_warps(kTmaLoad);
     constexpr int MMA_WARP = LOAD_WARPS;
     constexpr int EPI_WARP0 = LOAD_WARPS + 1;
+    using Lay = Layout<kTmaLoad>;
+    constexpr int NST = Lay::stages;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
 
-    const uint32_t sA = base + OFF_A;
-    const uint32_t sB = base + OFF_B;
-    const uint32_t bar0 = base + OFF_BAR;
+    const uint32_t sA = base + Lay::off_a;
+    const uint32_t sB = base + Lay::off_b;
+    const uint32_t bar0 = base + Lay::off_bar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + NUM_ACC + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * NUM_ACC);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_TMEM_SLOT);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (NST + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NST + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NST + NUM_ACC + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * NST + 2 * NUM_ACC);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::off_tmem_slot);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NST; ++s) {
             mbar_init(full_bar(s), kTmaLoad ? 1 : LOAD_WARPS * 32);
             mbar_init(empty_bar(s), 1);
         }
@@ -474,6 +652,7 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
             mbar_init(tempty_bar(a), EPI_WARPS * 32);
         }
         mbar_init(drain_bar, 1);
+        for (int q = 0; q < Lay::copy_slots; ++q) mbar_init(bar0 + 8u * (Lay::copy_bar0 + q), 1);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {
@@ -483,6 +662,12 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
     if (kTmaLoad && warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+    }
+    if constexpr (!kTmaLoad) {
+        if (warp == 0 && lane < 2 * MAX_CLASSES) {  // the maps of classes that hold rows
+            const int op = lane / MAX_CLASSES, cls = lane % MAX_CLASSES;
+            if ((p.cls_live[op] >> cls) & 1u) prefetch_tensormap(op == 0 ? &cm.a[cls] : &cm.b[cls]);
+        }
     }
     if (kTmaStore && warp == EPI_WARP0 && lane == 0) prefetch_tensormap(&tmC);
     tc_fence_before();
@@ -495,7 +680,7 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
 
     if (warp < LOAD_WARPS) {
         // ============================================================ producer
-        if (kTmaLoad) {
+        if constexpr (kTmaLoad) {
             if (lane == 0) {
                 uint32_t stage = 0, phase = 0;
                 uint32_t issued = 0;
@@ -531,43 +716,65 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                                 tma_load_2d(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK, k0, fb);
                         }
                         ++issued;
-                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                        if (++stage == NST) { stage = 0; phase ^= 1u; }
                     }
                 }
                 if (!ok) {
                     // Let the copies this thread started land before the CTA exits.
-                    const uint32_t n = issued < STAGES ? issued : STAGES;
+                    const uint32_t n = issued < NST ? issued : NST;
                     for (uint32_t q = issued - n; q < issued; ++q)
-                        mbar_wait_slow(full_bar(q % STAGES), (q / STAGES) & 1u, cleanup_wait(p.wait),
+                        mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u, cleanup_wait(p.wait),
                                        false);
                 }
             }
             __syncwarp();
         } else {
-            const int tid = threadIdx.x;  // 0 .. LOAD_WARPS*32-1
-            constexpr int NT = LOAD_WARPS * 32;
+            // Per-warp pipeline over this warp's copy groups: lane 0 keeps up to
+            // COPY_DEPTH groups of TMA copies in flight into the warp's staging
+            // ring while the warp places the oldest one into the stage. With
+            // cross-tile off, copies stop at each tile boundary until the
+            // previous tile's accumulator has been drained.
+            const uint32_t ring = base + Lay::off_copy + uint32_t(warp) * (COPY_DEPTH * GROUP_BYTES);
+            auto copy_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::copy_bar0 + warp * COPY_DEPTH + q); };
+            LineCursor iss, fix;
+            iss.start(blockIdx.x, p);
+            fix = iss;
+            uint32_t issued = 0, placed = 0;
             uint32_t stage = 0, phase = 0;
-            int32_t it = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += grid, ++it) {
-                int32_t tm, tn;
-                tile_coords(tile, p.sched, tm, tn);
-                if (!p.cross_tile && it > 0) {
-                    const int32_t j = it - 1;
+            while (fix.valid(p)) {
+                if (fix.g == 0 && fix.kb == 0 && !p.cross_tile && fix.it > 0) {
+                    const int32_t j = fix.it - 1;
                     if (!mbar_wait(tempty_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
                 }
-                const int64_t m0 = int64_t(tm) * BM, n0 = int64_t(tn) * BN;
-                for (int32_t kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
-                    const int64_t k0 = int64_t(kb) * BK;
-                    load_operand_tile<BM>(sA + stage * A_STAGE_BYTES, p.A, m0, p.M, k0, p.K, p.sam,
-                                          p.sak, p.a_mn, tid, NT);
-                    load_operand_tile<BN>(sB + stage * B_STAGE_BYTES, p.B, n0, p.N, k0, p.K, p.sbn,
-                                          p.sbk, p.b_mn, tid, NT);
-                    fence_proxy_async_smem();
-                    mbar_arrive(full_bar(stage));
-                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                while (issued - placed < COPY_DEPTH && iss.valid(p) && (p.cross_tile || iss.it == fix.it)) {
+                    const uint32_t q = issued % COPY_DEPTH;
+                    issue_class_group(p, cm, iss, warp + PRED_LOAD_WARPS * iss.g, ring + q * GROUP_BYTES,
+                                      copy_bar(q), lane);
+                    iss.next(p, grid);
+                    ++issued;
                 }
+                if (fix.g == 0 && !mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
+                const uint32_t q = placed % COPY_DEPTH;
+                if (!mbar_wait(copy_bar(q), (placed / COPY_DEPTH) & 1u, p.wait)) { ok = false; break; }
+                const int gamma = warp + PRED_LOAD_WARPS * fix.g;
+                const GroupShape gs = group_shape(p, gamma, fix.m0, fix.n0);
+                const uint32_t dst = gs.op == 0 ? sA + stage * A_STAGE_BYTES : sB + stage * B_STAGE_BYTES;
+                place_class_group(p, gs, ring + q * GROUP_BYTES, dst, lane);
+                __syncwarp();  // slot q is free for the next copies into it
+                if (fix.g == WARP_GROUPS - 1) {
+                    fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                    mbar_arrive(full_bar(stage));
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
+                }
+                fix.next(p, grid);
+                ++placed;
+            }
+            if (!ok) {
+                // Let the copies this warp started land before the CTA exits.
+                for (uint32_t q = placed; q < issued; ++q)
+                    mbar_wait_slow(copy_bar(q % COPY_DEPTH), (q / COPY_DEPTH) & 1u, cleanup_wait(p.wait),
+                                   false);
             }
         }
     } else if (warp == MMA_WARP) {
@@ -602,7 +809,7 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                     mma_f16_elect(d_tmem, a0 + k16 * da.k16, b0 + k16 * db.k16, idesc,
                                   (kb | k16) != 0 ? 1u : 0u);
                 mma_commit_elect(empty_bar(stage));  // slot reusable once these MMAs finish
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                if (++stage == NST) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
             mma_commit_elect(tfull_bar(acc));  // accumulator complete
@@ -614,7 +821,7 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
         // ============================================================ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access = tile rows q*32..q*32+31
         const int ew = warp - EPI_WARP0;
-        const uint32_t stg = base + OFF_EPI + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
+        const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         uint32_t buf = 0;
         int32_t it = 0;
         for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += grid, ++it) {

@@ -84,7 +84,12 @@ typedef enum {
  * Operands whose base address is 16-byte aligned and whose non-unit stride is
  * a multiple of 8 elements (A, B) or 4 elements (C) go through TMA; others
  * (e.g. K = 257 row-major) through a predicated load/store path with the same
- * results. With TMA-loadable A and B the work is split into 256x256 output
+ * results. On that path the rows of A and B are copied per alignment class
+ * (rows whose start shares its offset in a 16-byte granule), from the granule
+ * boundary below each row start: it may read, and discard, bytes that share
+ * an aligned 16-byte granule with an element of A or B, never others. If the
+ * driver rejects such a class description -> GEMM_ERR_UNSUPPORTED.
+ * With TMA-loadable A and B the work is split into 256x256 output
  * tiles, each computed by a pair of CTAs on the two SMs of a TPC (tcgen05
  * cta_group::2); otherwise, or with GEMM_SCHED_SINGLE_CTA, into 128x256 tiles
  * of one CTA each. The tile order (row-major / grouped) applies to whichever
