@@ -49,10 +49,10 @@ constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KiB
 constexpr int MN_CHUNK = 64;                // MN elements per 128-byte swizzle row
 constexpr int MN_CHUNK_BYTES = MN_CHUNK * BK * 2;  // 8 KiB: one MN-major TMA box
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;                       // two per TMEM lane quarter
 constexpr int EPI_COLS = 32;                       // fp32 columns per epilogue chunk
 constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 4;   // 32 rows x 128 B
-constexpr int EPI_BUFS = 2;
+constexpr int EPI_BUFS = 1;
 
 // Predicated-load path: for operands that one tensor map cannot describe (a
 // row stride or a base address that is not a multiple of 16 bytes).
@@ -455,13 +455,14 @@ __device__ __forceinline__ void place_class_group(const Params &p, const GroupSh
 }
 
 // ------------------------------------------------------------------ epilogue
-// Drains one accumulator of this CTA to C: the calling warp reads TMEM lanes
-// t_row.lane .. +31 (tile rows row0 .. row0+31) across BN columns in chunks of
-// 32, and writes C[row0 + r][col_base + c] for rows < M and columns < N.
-// TMA store: 128-byte-swizzled staging (two buffers per warp) + bulk tensor
+// Drains one accumulator of this CTA to C. Two warps share each TMEM lane
+// quarter (tile rows row0 .. row0+31): warp half h takes accumulator columns
+// [128h, 128h + 128). The TMEM load of the next 32 columns is issued before the
+// current ones are stored, so its latency overlaps the store work.
+// TMA store: 128-byte-swizzled staging (one buffer per warp) + bulk tensor
 // store, which clips the M/N edges. Otherwise: transpose through the staging
 // buffer so each store instruction writes 32 consecutive floats of one row.
-// `drained()` runs on every lane right after the last TMEM load of the tile.
+// `drained()` runs on every lane right after the warp's last TMEM load.
 //
 // Pacing: every program walks the same tile sequence in step, so without it all
 // epilogues would write their C tiles in the same few microseconds, a burst that
@@ -471,66 +472,106 @@ __device__ __forceinline__ void place_class_group(const Params &p, const GroupSh
 // activity 89 % -> 92 %.
 // Without cross-tile overlap the producer waits for the epilogue, so there is
 // nothing to spread the stores over.
-__device__ __forceinline__ uint32_t epilogue_pace_ns(int32_t unit_kblocks, uint32_t cross_tile) {
-    return (cross_tile && unit_kblocks >= 32) ? uint32_t(unit_kblocks) * 20u : 0u;
+constexpr int EPI_CHUNKS32 = BN / EPI_COLS;  // 8 fp32 chunks of 32 columns per accumulator row block
+constexpr int EPI_CHUNKS16 = BN / 64;        // 4 chunks of 64 16-bit values
+// Work units shorter than this many K-blocks split each row block's chunks
+// between its two epilogue warps (the drain is then on the critical path);
+// longer ones leave the second warp idle, which measured faster (less
+// interference with the MMA issue and the operand traffic): 16384^2 x K on
+// CTA pairs, two warps vs one per row block: K = 128 184 vs 202 us, K = 512
+// 258 vs 274 us, K = 1024 401 vs 380 us.
+constexpr int EPI_SPLIT_MAX_KB = 12;
+static_assert(EPI_WARPS == 8, "two epilogue warps per TMEM lane quarter");
+
+// Chunk range [c0, c0 + n) of the calling warp (n even, or 0).
+__device__ __forceinline__ void epilogue_chunks(int32_t unit_kblocks, int half, int chunks, int &c0, int &n) {
+    if (unit_kblocks < EPI_SPLIT_MAX_KB) {
+        n = chunks / 2;
+        c0 = half * n;
+    } else {
+        n = half == 0 ? chunks : 0;
+        c0 = 0;
+    }
+}
+
+__device__ __forceinline__ uint32_t epilogue_pace_ns(int32_t unit_kblocks, uint32_t cross_tile,
+                                                     int chunks_per_warp) {
+    // about 160 ns per K-block of spread over a warp's chunks
+    return (cross_tile && unit_kblocks >= 32 && chunks_per_warp > 0)
+               ? uint32_t(unit_kblocks) * 160u / uint32_t(chunks_per_warp)
+               : 0u;
+}
+
+// Stores one 32 x 32 fp32 chunk (this lane's row, 32 columns from col0).
+template <bool kTmaStore>
+__device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, int64_t col0, const Params &p,
+                                              const CUtensorMap *tmC, uint32_t stg, int lane, int32_t split) {
+    if (p.alpha != 1.0f) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(p.alpha * __uint_as_float(v[i]));
+    }
+    if (kTmaStore) {
+        if (lane == 0) bulk_wait_group_read<0>();  // the buffer's previous store has read it
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (row0 < p.M && col0 < p.N) {
+                if (p.splits > 1)  // partial tile -> workspace slice `split`, read once by the reduction
+                    tma_store_3d_hint(tmC, stg, int32_t(col0), int32_t(row0), split, l2_policy_evict_normal());
+                else if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
+                    tma_store_2d_hint(tmC, stg, int32_t(col0), int32_t(row0), l2_policy_evict_first());
+                else
+                    tma_store_2d(tmC, stg, int32_t(col0), int32_t(row0));
+            }
+            bulk_commit_group();
+        }
+    } else {
+        __syncwarp();  // every lane has read the buffer's previous contents
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        __syncwarp();
+        // all 32 staging reads first, so that no read waits behind a store
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+        const int64_t col = col0 + lane, rows = p.M - row0;
+        if (col < p.N) {
+            float *dst = p.C + row0 * p.scm + col;
+#pragma unroll
+            for (int r = 0; r < 32; ++r)
+                if (r < rows) dst[r * p.scm] = __uint_as_float(v[r]);
+        }
+    }
 }
 
 template <bool kTmaStore, typename Drained>
-__device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int64_t col_base,
-                                              const Params &p, const CUtensorMap *tmC, uint32_t stg,
-                                              uint32_t &buf, int lane, Drained drained,
-                                              int32_t split = 0, uint32_t pace_ns = 0) {
+__device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int64_t col_base, int c0, int n,
+                                              const Params &p, const CUtensorMap *tmC, uint32_t stg, int lane,
+                                              Drained drained, int32_t split = 0, uint32_t pace_ns = 0) {
+    if (n == 0) {
+        drained();
+        return;
+    }
+    uint32_t va[32], vb[32];
+    tmem_ld_32x32b_x32(t_row + c0 * EPI_COLS, va);
 #pragma unroll 1
-    for (int c = 0; c < BN / EPI_COLS; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(t_row + c * EPI_COLS, v);
+    for (int c = c0; c < c0 + n; c += 2) {
         tmem_ld_wait();
-        if (c == BN / EPI_COLS - 1) drained();
-        if (p.alpha != 1.0f) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(p.alpha * __uint_as_float(v[i]));
-        }
-        const int64_t col0 = col_base + c * EPI_COLS;
-        if (kTmaStore) {
-            const uint32_t dst = stg + buf * EPI_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();  // buffer free again
-            __syncwarp();
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4(dst + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (row0 < p.M && col0 < p.N) {
-                    if (p.splits > 1)  // partial tile -> workspace slice `split`, read once by the reduction
-                        tma_store_3d_hint(tmC, dst, int32_t(col0), int32_t(row0), split,
-                                          l2_policy_evict_normal());
-                    else if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
-                        tma_store_2d_hint(tmC, dst, int32_t(col0), int32_t(row0), l2_policy_evict_first());
-                    else
-                        tma_store_2d(tmC, dst, int32_t(col0), int32_t(row0));
-                }
-                bulk_commit_group();
-            }
-            buf ^= 1u;
-            if (pace_ns != 0 && c < BN / EPI_COLS - 1) __nanosleep(pace_ns);
-        } else {
-            __syncwarp();
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-            __syncwarp();
-            // all 32 staging reads first, so that no read waits behind a store
-#pragma unroll
-            for (int r = 0; r < 32; ++r) v[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
-            const int64_t col = col0 + lane, rows = p.M - row0;
-            if (col < p.N) {
-                float *dst = p.C + row0 * p.scm + col;
-#pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    if (r < rows) dst[r * p.scm] = __uint_as_float(v[r]);
-            }
-        }
+        tmem_ld_32x32b_x32(t_row + (c + 1) * EPI_COLS, vb);
+        store_chunk32<kTmaStore>(va, row0, col_base + c * EPI_COLS, p, tmC, stg, lane, split);
+        if (pace_ns != 0) __nanosleep(pace_ns);
+        tmem_ld_wait();
+        const bool more = c + 2 < c0 + n;
+        if (more)
+            tmem_ld_32x32b_x32(t_row + (c + 2) * EPI_COLS, va);
+        else
+            drained();
+        store_chunk32<kTmaStore>(vb, row0, col_base + (c + 1) * EPI_COLS, p, tmC, stg, lane, split);
+        if (pace_ns != 0 && more) __nanosleep(pace_ns);
     }
 }
 
@@ -545,69 +586,81 @@ __device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, uint32_t dtype
     return *reinterpret_cast<const uint32_t *>(&b);
 }
 
-// 16-bit C: like epilogue_tile, but 64 columns per chunk (two 32-column TMEM
-// loads), scaled by alpha and rounded, so that each staging row is again 128
-// bytes; the TMA store box is 64 x 32 elements of the 16-bit type.
-template <bool kTmaStore, typename Drained>
-__device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, int64_t col_base,
-                                                const Params &p, const CUtensorMap *tmC, uint32_t stg,
-                                                uint32_t &buf, int lane, Drained drained,
-                                                uint32_t pace_ns = 0) {
-    const float alpha = p.alpha;
-#pragma unroll 1
-    for (int c = 0; c < BN / 64; ++c) {
-        uint32_t v[32], w[32];
-        tmem_ld_32x32b_x32(t_row + c * 64, v);
-        tmem_ld_wait();
+__device__ __forceinline__ void pack_half_chunk(const uint32_t (&v)[32], uint32_t *w, float alpha,
+                                                uint32_t dtype) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            w[i] = pack_16x2(alpha * __uint_as_float(v[2 * i]), alpha * __uint_as_float(v[2 * i + 1]),
-                             p.out_dtype);
-        tmem_ld_32x32b_x32(t_row + c * 64 + 32, v);
-        tmem_ld_wait();
-        if (c == BN / 64 - 1) drained();
+    for (int i = 0; i < 16; ++i)
+        w[i] = pack_16x2(alpha * __uint_as_float(v[2 * i]), alpha * __uint_as_float(v[2 * i + 1]), dtype);
+}
+
+// Stores one chunk of 32 rows x 64 16-bit values (one 128-byte staging row per
+// lane; the TMA box is 64 x 32 elements).
+template <bool kTmaStore>
+__device__ __forceinline__ void store_chunk16(uint32_t (&w)[32], int64_t row0, int64_t col0, const Params &p,
+                                              const CUtensorMap *tmC, uint32_t stg, int lane) {
+    if (kTmaStore) {
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            w[16 + i] = pack_16x2(alpha * __uint_as_float(v[2 * i]),
-                                  alpha * __uint_as_float(v[2 * i + 1]), p.out_dtype);
-        const int64_t col0 = col_base + c * 64;
-        if (kTmaStore) {
-            const uint32_t dst = stg + buf * EPI_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<EPI_BUFS - 1>();
-            __syncwarp();
+        for (int u = 0; u < 8; ++u)
+            st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (row0 < p.M && col0 < p.N)
+                tma_store_2d_hint(tmC, stg, int32_t(col0), int32_t(row0), l2_policy_evict_first());
+            bulk_commit_group();
+        }
+    } else {
+        __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4(dst + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (row0 < p.M && col0 < p.N)
-                    tma_store_2d_hint(tmC, dst, int32_t(col0), int32_t(row0), l2_policy_evict_first());
-                bulk_commit_group();
-            }
-            buf ^= 1u;
-            if (pace_ns != 0 && c < BN / 64 - 1) __nanosleep(pace_ns);
-        } else {
-            __syncwarp();
+        for (int u = 0; u < 8; ++u)
+            st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            __syncwarp();
+        for (int r = 0; r < 32; ++r) w[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
+        const int64_t col = col0 + 2 * lane, rows = p.M - row0;  // this lane: columns col, col + 1
+        if (col < p.N) {
+            uint16_t *dst = reinterpret_cast<uint16_t *>(p.C) + row0 * p.scm + col;
+            const bool both = col + 1 < p.N;
 #pragma unroll
-            for (int r = 0; r < 32; ++r) w[r] = ld_shared_b32(stg + swz128(r, lane >> 2) + (lane & 3) * 4);
-            const int64_t col = col0 + 2 * lane, rows = p.M - row0;  // this lane: columns col, col + 1
-            if (col < p.N) {
-                uint16_t *dst = reinterpret_cast<uint16_t *>(p.C) + row0 * p.scm + col;
-                const bool both = col + 1 < p.N;
-#pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    if (r < rows) {
-                        dst[r * p.scm] = uint16_t(w[r] & 0xffffu);
-                        if (both) dst[r * p.scm + 1] = uint16_t(w[r] >> 16);
-                    }
+            for (int r = 0; r < 32; ++r) {
+                if (r < rows) {
+                    dst[r * p.scm] = uint16_t(w[r] & 0xffffu);
+                    if (both) dst[r * p.scm + 1] = uint16_t(w[r] >> 16);
                 }
             }
         }
+    }
+}
+
+// 16-bit C: like epilogue_tile, with chunks of 64 columns (two 32-column TMEM
+// loads), scaled by alpha and rounded.
+template <bool kTmaStore, typename Drained>
+__device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, int64_t col_base, int c0, int n,
+                                                const Params &p, const CUtensorMap *tmC, uint32_t stg,
+                                                int lane, Drained drained, uint32_t pace_ns = 0) {
+    if (n == 0) {
+        drained();
+        return;
+    }
+    const float alpha = p.alpha;
+    uint32_t va[32], vb[32], w[32];
+    tmem_ld_32x32b_x32(t_row + c0 * 64, va);
+#pragma unroll 1
+    for (int c = c0; c < c0 + n; ++c) {
+        tmem_ld_wait();
+        tmem_ld_32x32b_x32(t_row + c * 64 + 32, vb);
+        pack_half_chunk(va, w, alpha, p.out_dtype);
+        tmem_ld_wait();
+        const bool more = c + 1 < c0 + n;
+        if (more)
+            tmem_ld_32x32b_x32(t_row + (c + 1) * 64, va);
+        else
+            drained();
+        pack_half_chunk(vb, w + 16, alpha, p.out_dtype);
+        store_chunk16<kTmaStore>(w, row0, col_base + c * 64, p, tmC, stg, lane);
+        if (pace_ns != 0 && more) __nanosleep(pace_ns);
     }
 }
 
@@ -821,8 +874,8 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
         // ============================================================ epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access = tile rows q*32..q*32+31
         const int ew = warp - EPI_WARP0;
+        const int half = ew / 4;  // which of the two warps of its TMEM lane quarter
         const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
-        uint32_t buf = 0;
         int32_t it = 0;
         for (int32_t tile = blockIdx.x; tile < p.num_tiles; tile += grid, ++it) {
             int32_t tm, tn;
@@ -839,12 +892,17 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                 tc_fence_before();
                 mbar_arrive(tempty_bar(acc));  // accumulator may be overwritten
             };
-            if (p.out_dtype == 0)
-                epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane, release,
-                                         0, epilogue_pace_ns(num_kb, p.cross_tile));
-            else
-                epilogue_tile16<kTmaStore>(t_row, row0, int64_t(tn) * BN, p, &tmC, stg, buf, lane,
-                                           release, epilogue_pace_ns(num_kb, p.cross_tile));
+            const int64_t col_base = int64_t(tn) * BN;
+            int c0, n;
+            if (p.out_dtype == 0) {
+                epilogue_chunks(num_kb, half, EPI_CHUNKS32, c0, n);
+                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, 0,
+                                         epilogue_pace_ns(num_kb, p.cross_tile, n));
+            } else {
+                epilogue_chunks(num_kb, half, EPI_CHUNKS16, c0, n);
+                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
+                                           epilogue_pace_ns(num_kb, p.cross_tile, n));
+            }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -230,13 +230,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         // ============================================================ epilogue (both CTAs)
         const int q = warp & 3;
         const int ew = warp - EPI_WARP0;
+        const int half = ew / 4;
         const uint32_t stg = base + pair::OFF_EPI + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
-        uint32_t buf = 0;
         int32_t it = 0;
         for (int32_t u = pair_id; u < p.num_units; u += num_pairs, ++it) {
             const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
             const int32_t kb0 = split * p.kb_per_split;
-            const uint32_t pace = epilogue_pace_ns(min(num_kb, kb0 + p.kb_per_split) - kb0, p.cross_tile);
+            const int32_t unit_kb = min(num_kb, kb0 + p.kb_per_split) - kb0;
             int32_t tm, tn;
             tile_coords(tile, p.sched, tm, tn);
             const uint32_t acc = it & 1, use = it >> 1;
@@ -253,12 +253,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                     mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
                 }
             };
-            if (p.out_dtype == 0 || p.splits > 1)  // split-K partials are fp32
-                epilogue_tile<kTmaStore>(t_row, row0, int64_t(tn) * pair::TILE_N, p, &tmC, stg, buf, lane,
-                                         release, split, pace);
-            else
-                epilogue_tile16<kTmaStore>(t_row, row0, int64_t(tn) * pair::TILE_N, p, &tmC, stg, buf,
-                                           lane, release, pace);
+            const int64_t col_base = int64_t(tn) * pair::TILE_N;
+            int c0, n;
+            if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
+                epilogue_chunks(unit_kb, half, EPI_CHUNKS32, c0, n);
+                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split,
+                                         epilogue_pace_ns(unit_kb, p.cross_tile, n));
+            } else {
+                epilogue_chunks(unit_kb, half, EPI_CHUNKS16, c0, n);
+                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
+                                           epilogue_pace_ns(unit_kb, p.cross_tile, n));
+            }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

@@ -129,6 +129,10 @@ def test_non_persistent_grid_bit_exact(shape, grouped, single):
     ("misaligned C base", 129, 256, 64, ("row", 0, 0), ("row", 0, 0), (256, 1)),
     ("all predicated", 131, 259, 67, ("col", 1, 1), ("col", 3, 1), (263, 3)),
     ("pair tiles, predicated store", 300, 520, 128, ("row", 0, 0), ("col", 0, 0), (523, 1)),
+    # alignment classes with no rows: K < 8 rows of M/N-major operands, M < 8 rows of K-major A
+    ("tiny K, M- and N-major odd strides", 70, 90, 3, ("col", 1, 0), ("row", 1, 1), None),
+    ("tiny M, odd K", 3, 300, 101, ("row", 0, 0), ("row", 0, 0), None),
+    ("N-major B, stride 4 mod 8", 150, 200, 70, ("row", 2, 0), ("row", 4, 0), None),
 ])
 def test_predicated_paths_bit_exact(case):
     name, M, N, K, la, lb, lc = case
@@ -216,10 +220,13 @@ def test_invalid_arguments_raise():
 
 
 def test_kernel_resources():
+    # warps: producer (1, or 3 for predicated loads) + MMA + 8 epilogue
+    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320}
     for v in range(6):
         info = kernel_info(v)
         assert info["dynamic_smem"] <= 232448 and info["regs_per_thread"] <= 255
-        assert info["threads_per_cta"] in (192, 288)
+        assert info["threads_per_cta"] == threads[v]
+        assert info["threads_per_cta"] * info["regs_per_thread"] <= 65536  # one CTA per SM fits
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert get_config(16384, 16384, single_cta=True)["grid"] == sms
     pairs = get_config(16384, 16384)["grid"]
