@@ -29,7 +29,8 @@ struct DeviceState {
     std::once_flag once;
     cudaError_t init_err = cudaSuccess;
     int num_sms = 0;
-    int max_pairs = 0;  // co-resident 2-CTA clusters of the pair kernel
+    int max_pairs = 0;       // co-resident 2-CTA clusters of the pair kernel (TMA loads)
+    int max_pairs_pred = 0;  // the same for its predicated-load variant
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -54,13 +55,15 @@ cudaError_t set_smem_attr() {
                                 Layout<L>::smem_bytes);
 }
 
-template <bool S>
+template <bool L, bool S>
 cudaError_t set_pair_smem_attr() {
-    return cudaFuncSetAttribute(gemm_f16_pair<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                pair::SMEM_BYTES);
+    return cudaFuncSetAttribute(gemm_f16_pair<L, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                pair::Layout<L>::smem_bytes);
 }
 
-// How many 2-CTA clusters of the pair kernel fit on the device at once.
+// How many 2-CTA clusters of the pair kernel (TMA-load variant L = true, or
+// predicated-load variant) fit on the device at once.
+template <bool L>
 int query_max_pairs(int num_sms) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -69,12 +72,12 @@ int query_max_pairs(int num_sms) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(pair::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.blockDim = dim3(pair::Layout<L>::threads, 1, 1);
+    cfg.dynamicSmemBytes = pair::Layout<L>::smem_bytes;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_pair<true>, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_f16_pair<L, true>, &cfg) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = num_sms / 2;
     }
@@ -90,9 +93,12 @@ cudaError_t device_init(int dev, DeviceState **out) {
         if (e == cudaSuccess) e = set_smem_attr<true, false>();
         if (e == cudaSuccess) e = set_smem_attr<false, true>();
         if (e == cudaSuccess) e = set_smem_attr<false, false>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<true>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<false>();
-        if (e == cudaSuccess) d.max_pairs = query_max_pairs(d.num_sms);
+        if (e == cudaSuccess) e = set_pair_smem_attr<true, true>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<true, false>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<false, true>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<false, false>();
+        if (e == cudaSuccess) d.max_pairs = query_max_pairs<true>(d.num_sms);
+        if (e == cudaSuccess) d.max_pairs_pred = query_max_pairs<false>(d.num_sms);
         d.init_err = e;
     });
     *out = &d;
@@ -133,11 +139,14 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, ui
 // rows start m_c bytes early, at the granule boundary, and whose width grows by
 // m_c/2 elements. Every byte TMA reads through these maps therefore shares its
 // granule with an element of the operand. Returns false if a map is rejected.
-bool encode_classes(CUtensorMap *maps, const void *X, int64_t S, int64_t rows, int64_t cols,
-                    uint32_t *P_out, uint32_t *mis, uint32_t *live) {
+bool encode_classes(CUtensorMap *maps, const void *X, int64_t S, int64_t rows, int64_t cols, bool mn_major,
+                    uint32_t *lp_out, uint32_t *lh_out, uint32_t *mis, uint32_t *live) {
     const uint64_t r = (2u * uint64_t(S)) % 16u;
     const uint64_t P = r == 0 ? 1u : 16u / std::gcd(r, uint64_t(16));
-    *P_out = uint32_t(P);
+    const int lp = __builtin_ctzll(P);
+    const int lh = class_box_lh(mn_major, lp);
+    *lp_out = uint32_t(lp);
+    *lh_out = uint32_t(lh);
     *mis = 0;
     *live = 0;
     for (uint64_t c = 0; c < P; ++c) {
@@ -146,7 +155,7 @@ bool encode_classes(CUtensorMap *maps, const void *X, int64_t S, int64_t rows, i
         const uintptr_t a = reinterpret_cast<uintptr_t>(X) + 2u * uint64_t(S) * c;
         const uint32_t m = uint32_t(a & 15u);
         if (!encode_2d(&maps[c], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, reinterpret_cast<const void *>(a - m),
-                       uint64_t(cols) + m / 2u, nrows, 2u * uint64_t(S) * P, BOX_W, BOX_H,
+                       uint64_t(cols) + m / 2u, nrows, 2u * uint64_t(S) * P, BOX_W, 1u << lh,
                        CU_TENSOR_MAP_SWIZZLE_NONE))
             return false;
         *mis |= m << (4u * c);
@@ -193,14 +202,17 @@ cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap
     return cudaGetLastError();
 }
 
-template <bool S>
-cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c,
-                        const Params &p, int grid, cudaStream_t stream) {
-    gemm_f16_pair<S><<<grid, pair::THREADS, pair::SMEM_BYTES, stream>>>(a, b, c, p);
+template <bool L, bool S>
+cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
+                        const ClassMaps &cm, int grid, cudaStream_t stream) {
+    constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
+    if constexpr (L)
+        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, p, NoClassMaps{});
+    else
+        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, p, cm);
     return cudaGetLastError();
 }
 
-// Tile shape of the kernel that `flags` selects for TMA-loadable operands.
 void tile_shape(uint32_t flags, int *bm, int *bn) {
     const bool single = (flags & GEMM_SCHED_SINGLE_CTA) != 0;
     *bm = single ? BM : pair::TILE_M;
@@ -317,8 +329,8 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     const bool load_tma = a_tma && b_tma;
     const bool store_tma = tma_ok(C, N, stride_cm, esize);
     // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
-    const bool use_pair = load_tma && !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
-    if (sk.enabled && !use_pair) return GEMM_ERR_UNSUPPORTED;  // split-K runs on CTA pairs with TMA loads
+    const bool use_pair = !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
+    if (sk.enabled && !(use_pair && load_tma)) return GEMM_ERR_UNSUPPORTED;  // split-K: CTA pairs, TMA loads
     const int tile_m = use_pair ? pair::TILE_M : BM;
     const int tile_n = use_pair ? pair::TILE_N : BN;
     const int cta_m = use_pair ? pair::CTA_M : BM;    // A rows one CTA loads
@@ -344,12 +356,16 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     static_assert(sizeof(ClassMaps) == 2 * MAX_CLASSES * sizeof(CUtensorMap), "");
     ClassMaps cm;
     std::memset(&cm, 0, sizeof(cm));
-    uint32_t cls_p[2] = {1, 1}, cls_mis[2] = {0, 0}, cls_live[2] = {0, 0};
+    uint32_t cls_lp[2] = {0, 0}, cls_lh[2] = {4, 4}, cls_mis[2] = {0, 0}, cls_live[2] = {0, 0};
     if (!load_tma) {
-        const bool okA = a_k ? encode_classes(cm.a, A, stride_am, M, K, &cls_p[0], &cls_mis[0], &cls_live[0])
-                             : encode_classes(cm.a, A, stride_ak, K, M, &cls_p[0], &cls_mis[0], &cls_live[0]);
-        const bool okB = b_n ? encode_classes(cm.b, B, stride_bk, K, N, &cls_p[1], &cls_mis[1], &cls_live[1])
-                             : encode_classes(cm.b, B, stride_bn, N, K, &cls_p[1], &cls_mis[1], &cls_live[1]);
+        const bool okA = a_k ? encode_classes(cm.a, A, stride_am, M, K, false, &cls_lp[0], &cls_lh[0], &cls_mis[0],
+                                              &cls_live[0])
+                             : encode_classes(cm.a, A, stride_ak, K, M, true, &cls_lp[0], &cls_lh[0], &cls_mis[0],
+                                              &cls_live[0]);
+        const bool okB = b_n ? encode_classes(cm.b, B, stride_bk, K, N, true, &cls_lp[1], &cls_lh[1], &cls_mis[1],
+                                              &cls_live[1])
+                             : encode_classes(cm.b, B, stride_bn, N, K, false, &cls_lp[1], &cls_lh[1], &cls_mis[1],
+                                              &cls_live[1]);
         if (!okA || !okB) return GEMM_ERR_UNSUPPORTED;
     }
     SplitPlan sp{1, int32_t(cdiv(K, BK)), N};
@@ -404,7 +420,8 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     p.idesc = make_idesc(p.a_mn, p.b_mn, use_pair ? 2 * pair::CTA_M : BM, tile_n);
     p.cross_tile = (schedule_flags & GEMM_SCHED_CROSS_TILE) ? 1u : 0u;
     for (int op = 0; op < 2; ++op) {
-        p.cls_lp[op] = uint32_t(__builtin_ctz(cls_p[op]));
+        p.cls_lp[op] = cls_lp[op];
+        p.cls_lh[op] = cls_lh[op];
         p.cls_mis[op] = cls_mis[op];
         p.cls_live[op] = cls_live[op];
     }
@@ -421,7 +438,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     p.wait.epoch = next_epoch();
 
     const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT);
-    const int programs = !persistent ? p.num_units : use_pair ? ds->max_pairs : ds->num_sms;
+    const int programs = !persistent ? p.num_units
+                         : use_pair  ? (load_tma ? ds->max_pairs : ds->max_pairs_pred)
+                                     : ds->num_sms;
     const int grid_programs = int(p.num_units < programs ? p.num_units : programs);
     if (use_pair && int64_t(grid_programs) * 2 > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     const int grid = use_pair ? 2 * grid_programs : grid_programs;
@@ -438,7 +457,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
 
     cudaError_t e;
     if (split) {
-        e = launch_pair<true>(tmA, tmB, tmC, p, grid, stream);
+        e = launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
         if (e == cudaSuccess) {
             const int64_t quads = M * ((N + 3) / 4);
             const int threads = 256;
@@ -448,9 +467,14 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                                               sp.ldw, stride_cm, sp.splits, out_dtype, alpha);
             e = cudaGetLastError();
         }
-    } else if (use_pair)
-        e = store_tma ? launch_pair<true>(tmA, tmB, tmC, p, grid, stream)
-                      : launch_pair<false>(tmA, tmB, tmC, p, grid, stream);
+    } else if (use_pair) {
+        if (load_tma)
+            e = store_tma ? launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream)
+                          : launch_pair<true, false>(tmA, tmB, tmC, p, cm, grid, stream);
+        else
+            e = store_tma ? launch_pair<false, true>(tmA, tmB, tmC, p, cm, grid, stream)
+                          : launch_pair<false, false>(tmA, tmB, tmC, p, cm, grid, stream);
+    }
     else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
     else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, cm, grid, stream);
     else if (store_tma) e = launch<false, true>(tmA, tmB, tmC, p, cm, grid, stream);
@@ -559,24 +583,24 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
 
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
                                    int32_t *dynamic_smem, int32_t *threads) {
-    if (variant < 0 || variant > 5) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 7) return GEMM_ERR_INVALID_ARG;
     cudaFuncAttributes a;
     cudaError_t e;
-    int thr;
+    int thr, dyn;
     switch (variant) {
-        case 0: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, true>); thr = cta_threads(true); break;
-        case 1: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, false>); thr = cta_threads(true); break;
-        case 2: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, true>); thr = cta_threads(false); break;
-        case 3: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, false>); thr = cta_threads(false); break;
-        case 4: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true>); thr = pair::THREADS; break;
-        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false>); thr = pair::THREADS; break;
+        case 0: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, true>); thr = cta_threads(true); dyn = Layout<true>::smem_bytes; break;
+        case 1: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<true, false>); thr = cta_threads(true); dyn = Layout<true>::smem_bytes; break;
+        case 2: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, true>); thr = cta_threads(false); dyn = Layout<false>::smem_bytes; break;
+        case 3: e = cudaFuncGetAttributes(&a, gemm_f16_persistent<false, false>); thr = cta_threads(false); dyn = Layout<false>::smem_bytes; break;
+        case 4: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        case 5: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        case 6: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, true>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
     }
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;
     if (static_smem) *static_smem = int32_t(a.sharedSizeBytes);
-    if (dynamic_smem)
-        *dynamic_smem = variant >= 4 ? pair::SMEM_BYTES
-                        : variant >= 2 ? Layout<false>::smem_bytes : Layout<true>::smem_bytes;
+    if (dynamic_smem) *dynamic_smem = dyn;
     if (threads) *threads = thr;
     return GEMM_OK;
 }

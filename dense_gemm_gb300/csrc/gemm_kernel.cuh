@@ -63,22 +63,29 @@ constexpr int EPI_BUFS = 1;
 // alignment class c: they all start m_c bytes into a 16-byte granule, and two
 // consecutive rows of a class are 2*S*P bytes apart, a multiple of 16. Each
 // class gets its own tensor map whose rows begin at those granule boundaries,
-// so TMA copies boxes of 8 class rows x 72 elements (a line plus up to 7
-// leading elements) into a staging ring, with zero fill past the matrix
-// edges, and the loader warps shift each line by m_c bytes into the stage.
-constexpr int PRED_LOAD_WARPS = 3;
+// so TMA copies boxes of h class rows x 72 elements (a line plus up to 7
+// leading elements; h = 16, or 8 for an M/N-major operand with 8 classes)
+// into a staging ring, with zero fill past the matrix edges, and loader warps
+// shift each line by m_c bytes into the stage. A loader warp handles copy
+// groups of 64 lines.
 constexpr int MAX_CLASSES = 8;
 constexpr int BOX_W = 72;                           // elements per staged line
-constexpr int BOX_H = 8;                            // class rows per box
 constexpr int LINE_PITCH = BOX_W * 2;               // 144 bytes
-constexpr int BOX_BYTES = BOX_H * LINE_PITCH;       // 1152 = 9 x 128
-constexpr int GROUP_BOXES = 8;                      // 64 lines per copy group
-constexpr int GROUP_BYTES = GROUP_BOXES * BOX_BYTES;
+constexpr int GROUP_LINES = 64;
+constexpr int GROUP_BYTES = GROUP_LINES * LINE_PITCH;  // 9216 = 72 x 128
 constexpr int COPY_DEPTH = 3;                       // copy groups in flight per loader warp
-constexpr int A_GROUPS = BM / 64, B_GROUPS = BN / 64;
+// one-CTA kernel: three loader warps, two groups each per K-block
+constexpr int PRED_LOAD_WARPS = 3;
+constexpr int A_GROUPS = BM / GROUP_LINES, B_GROUPS = BN / GROUP_LINES;
 constexpr int GROUPS_PER_KB = A_GROUPS + B_GROUPS;  // 6
-constexpr int WARP_GROUPS = GROUPS_PER_KB / PRED_LOAD_WARPS;  // per loader warp and K-block
+constexpr int WARP_GROUPS = GROUPS_PER_KB / PRED_LOAD_WARPS;
 static_assert(GROUPS_PER_KB % PRED_LOAD_WARPS == 0, "equal loader shares");
+
+// log2 of the box height for an operand with 2^lp classes (host and device).
+__host__ __device__ constexpr int class_box_lh(bool mn_major, int lp) {
+    // rows per class in one 64-deep k-block tile: 64 / P (M/N-major) or >= 128 / P
+    return mn_major ? (6 - lp < 4 ? 6 - lp : 4) : 4;
+}
 
 // Shared-memory map of the one-CTA kernel. The predicated-load variant keeps
 // two operand stages and holds the loader warps' staging rings (with one
@@ -97,8 +104,8 @@ struct Layout {
     static constexpr int off_tmem_slot = off_bar + num_bars * 8;
     static constexpr int smem_bytes = off_tmem_slot + 16 + 1024;  // slack to align the base to 1 KiB
     static_assert(off_b % 1024 == 0 && off_epi % 1024 == 0, "swizzled buffers need 1 KiB alignment");
-    static_assert(off_copy % 128 == 0 && GROUP_BYTES % 128 == 0 && BOX_BYTES % 128 == 0,
-                  "TMA box destinations need 128-byte alignment");
+    static_assert(off_copy % 128 == 0 && GROUP_BYTES % 128 == 0 && (8 * LINE_PITCH) % 128 == 0,
+                  "TMA box destinations (multiples of 8 lines) need 128-byte alignment");
     static_assert(smem_bytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
 };
 
@@ -243,10 +250,11 @@ struct Params {
     uint32_t cross_tile;
     uint32_t l2_mode;   // bit 0: C stores evict-first; bit 1: A/B loads evict-last (pair kernel)
     uint32_t out_dtype; // C element type: 0 fp32, 1 fp16, 2 bf16 (nearest-even)
-    // predicated loads, per operand (0 = A, 1 = B): log2 of the class count P,
-    // each class's byte offset in its first granule (4 bits per class), and
-    // the classes that hold rows
+    // predicated loads, per operand (0 = A, 1 = B): log2 of the class count P
+    // and of the box height, each class's byte offset in its first granule (4
+    // bits per class), and the classes that hold rows
     uint32_t cls_lp[2];
+    uint32_t cls_lh[2];
     uint32_t cls_mis[2];
     uint32_t cls_live[2];
     float alpha;        // C = alpha * (A @ B)
@@ -341,17 +349,17 @@ struct LineCursor {
     }
 };
 
-// Copy group `gamma` (0 .. GROUPS_PER_KB-1) of a K-block: the first A_GROUPS
-// groups hold A's 128 lines, the rest B's 256, 64 lines (8 boxes) each. Box
-// beta of an operand covers class c, row block b (8 class rows) and 64-element
-// segment s, with s fastest: an operand has NS = R/64 segments per row when
-// M/N-major (rows are k) and 1 when K-major (rows are m or n).
+// Copy group g of one operand's 2^lr-line tile (lines 64g .. 64g+63) of a
+// K-block. Box beta of the operand covers class c, row block b (h class rows)
+// and 64-element segment s, s fastest: an operand has NS = R/64 segments per
+// row when M/N-major (rows are k, 64 per K-block) and 1 when K-major (rows are
+// m or n, R per tile).
 struct GroupShape {
-    int op;              // 0 = A, 1 = B
-    int first_box;       // beta of the group's first box
-    int lp, lns, lbc;    // log2 of: classes P, segments per row NS, row blocks per class
+    int op;                 // 0 = A, 1 = B
+    int first_box;          // beta of the group's first box
+    int lp, lns, lbc, lh;   // log2 of: classes P, segments per row NS, row blocks per class, box height
     uint32_t mn_major;
-    int64_t mn0;
+    int64_t mn0;            // first m (A) or n (B) of the tile
 
     // box beta -> class, row block, segment (all counts are powers of two)
     __device__ __forceinline__ int cls(int beta) const { return beta >> (lbc + lns); }
@@ -359,47 +367,42 @@ struct GroupShape {
     __device__ __forceinline__ int seg(int beta) const { return beta & ((1 << lns) - 1); }
 };
 
-__device__ __forceinline__ GroupShape group_shape(const Params &p, int gamma, int64_t m0, int64_t n0) {
+__device__ __forceinline__ GroupShape group_shape(const Params &p, int op, int g, int lr, int64_t mn0) {
     GroupShape gs;
-    const bool is_a = gamma < A_GROUPS;
-    gs.op = is_a ? 0 : 1;
-    gs.first_box = (is_a ? gamma : gamma - A_GROUPS) * GROUP_BOXES;
-    gs.mn_major = is_a ? p.a_mn : p.b_mn;
-    gs.lp = int(is_a ? p.cls_lp[0] : p.cls_lp[1]);
-    // R = 128 (A) or 256 (B) lines: NS = R/64 when M/N-major, else 1; rows per
-    // operand tile NR = 64 (k) when M/N-major, else R; Bc = NR / (8 P)
-    const int lr = is_a ? 7 : 8;
+    gs.op = op;
+    gs.mn_major = op == 0 ? p.a_mn : p.b_mn;
+    gs.lp = int(op == 0 ? p.cls_lp[0] : p.cls_lp[1]);
+    gs.lh = int(op == 0 ? p.cls_lh[0] : p.cls_lh[1]);
     gs.lns = gs.mn_major ? lr - 6 : 0;
-    gs.lbc = (gs.mn_major ? 6 : lr) - 3 - gs.lp;
-    gs.mn0 = is_a ? m0 : n0;
+    gs.lbc = (gs.mn_major ? 6 : lr) - gs.lp - gs.lh;  // rows per tile / (P h)
+    gs.first_box = g << (6 - gs.lh);                   // 64 / h boxes per group
+    gs.mn0 = mn0;
     return gs;
 }
 
 // Starts the TMA copies of one group into ring slot `slot`; they complete on
-// `bar`. Lane 0 announces the byte count, then lane i < 8 issues box i (boxes
-// of classes without rows are skipped and placed as zeros). Whole warp.
-__device__ __forceinline__ void issue_class_group(const Params &p, const ClassMaps &cm,
-                                                  const LineCursor &c, int gamma, uint32_t slot,
-                                                  uint32_t bar, int lane) {
-    const GroupShape gs = group_shape(p, gamma, c.m0, c.n0);
+// `bar`. Lane 0 announces the byte count, then lane i < 64/h issues box i
+// (boxes of classes without rows are skipped and placed as zeros). Whole warp.
+__device__ __forceinline__ void issue_class_group(const Params &p, const ClassMaps &cm, const GroupShape &gs,
+                                                  int64_t k0, uint32_t slot, uint32_t bar, int lane) {
     const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
+    const int nbox = GROUP_LINES >> gs.lh;
+    const uint32_t box_bytes = uint32_t(LINE_PITCH) << gs.lh;
     if (lane == 0) {
         uint32_t boxes = 0;
-#pragma unroll
-        for (int i = 0; i < GROUP_BOXES; ++i) boxes += (live >> gs.cls(gs.first_box + i)) & 1u;
+        for (int i = 0; i < nbox; ++i) boxes += (live >> gs.cls(gs.first_box + i)) & 1u;
         fence_proxy_async_smem();  // this slot's staging reads precede the new copies
-        mbar_arrive_expect_tx(bar, boxes * BOX_BYTES);
+        mbar_arrive_expect_tx(bar, boxes * box_bytes);
     }
     __syncwarp();
-    if (lane < GROUP_BOXES) {
-        const int64_t k0 = int64_t(c.kb) * BK;
+    if (lane < nbox) {
         const int32_t xb = int32_t(gs.mn_major ? gs.mn0 : k0);              // unit-stride coordinate
         const int32_t yb = int32_t((gs.mn_major ? k0 : gs.mn0) >> gs.lp);  // class row of the tile's first row
         const int beta = gs.first_box + lane, cls = gs.cls(beta);
         const CUtensorMap *maps = gs.op == 0 ? cm.a : cm.b;
         if ((live >> cls) & 1u)
-            tma_load_2d(slot + uint32_t(lane) * BOX_BYTES, &maps[cls], xb + 64 * gs.seg(beta),
-                        yb + BOX_H * gs.blk(beta), bar);
+            tma_load_2d(slot + uint32_t(lane) * box_bytes, &maps[cls], xb + 64 * gs.seg(beta),
+                        yb + (gs.blk(beta) << gs.lh), bar);
     }
 }
 
@@ -416,40 +419,37 @@ __device__ __forceinline__ void window16(const uint32_t (&w)[8], uint32_t m, uin
     for (int t = 0; t < 4; ++t) o[t] = __byte_perm(y[t], y[t + 1], sel);
 }
 
-// All lanes: shift the group's 64 staged lines (8 boxes of 8) into the operand
-// stage at `dst`. In step j of a pair of boxes, lane l moves 16 bytes: unit
-// l % 8 of line 4j + l / 8; each box has one class and thus one offset m.
+// All lanes: shift the group's 64 staged lines into the operand stage at
+// `dst`. In step k (0..15) lane l moves 16 bytes: unit l % 8 of staged line
+// 4k + l / 8. The four lines of a step lie in one box (h >= 8), hence share a
+// class and its offset m. Staging reads of four steps are issued first.
 __device__ __forceinline__ void place_class_group(const Params &p, const GroupShape &gs, uint32_t slot,
                                                   uint32_t dst, int lane) {
     const uint32_t mis = gs.op == 0 ? p.cls_mis[0] : p.cls_mis[1];
     const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
     const uint32_t u = uint32_t(lane) & 7u, r4 = uint32_t(lane) >> 3;
     const uint32_t seg_bytes = gs.mn_major ? uint32_t(MN_CHUNK_BYTES) : 0u;
+    const uint32_t hmask = (1u << gs.lh) - 1u;
 #pragma unroll 1
-    for (int bx = 0; bx < GROUP_BOXES; bx += 2) {
+    for (int k0 = 0; k0 < GROUP_LINES / 4; k0 += 4) {
         uint32_t w[4][8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // the staging reads of both boxes first
-            const uint32_t src = slot + (uint32_t(8 * bx + 4 * j) + r4) * LINE_PITCH + 16u * u;
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t src = slot + (uint32_t(4 * (k0 + j)) + r4) * LINE_PITCH + 16u * u;
             ld_shared_v4(src, w[j][0], w[j][1], w[j][2], w[j][3]);
             ld_shared_v4(src + 16u, w[j][4], w[j][5], w[j][6], w[j][7]);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int beta = gs.first_box + bx + h, cls = gs.cls(beta);
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t l = uint32_t(4 * (k0 + j)) + r4;
+            const int beta = gs.first_box + int(l >> gs.lh), cls = gs.cls(beta);
             const uint32_t m = (mis >> (4 * cls)) & 15u;  // where the lines start in their window
-            const bool has_rows = (live >> cls) & 1u;
-            const uint32_t row0 = uint32_t(BOX_H * gs.blk(beta));
-            const uint32_t seg_off = uint32_t(gs.seg(beta)) * seg_bytes;
-#pragma unroll
-            for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * h + jj;
-                uint32_t o[4];
-                window16(w[j], m, o);
-                if (!has_rows) o[0] = o[1] = o[2] = o[3] = 0u;
-                const uint32_t rho = uint32_t(cls) + ((row0 + 4u * uint32_t(jj) + r4) << gs.lp);
-                st_shared_v4(dst + seg_off + rho * 128u + ((u ^ (rho & 7u)) << 4), o[0], o[1], o[2], o[3]);
-            }
+            uint32_t o[4];
+            window16(w[j], m, o);
+            if (!((live >> cls) & 1u)) o[0] = o[1] = o[2] = o[3] = 0u;
+            const uint32_t rho = uint32_t(cls) + (((uint32_t(gs.blk(beta)) << gs.lh) + (l & hmask)) << gs.lp);
+            st_shared_v4(dst + uint32_t(gs.seg(beta)) * seg_bytes + rho * 128u + ((u ^ (rho & 7u)) << 4), o[0],
+                         o[1], o[2], o[3]);
         }
     }
 }
@@ -802,8 +802,11 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                 }
                 while (issued - placed < COPY_DEPTH && iss.valid(p) && (p.cross_tile || iss.it == fix.it)) {
                     const uint32_t q = issued % COPY_DEPTH;
-                    issue_class_group(p, cm, iss, warp + PRED_LOAD_WARPS * iss.g, ring + q * GROUP_BYTES,
-                                      copy_bar(q), lane);
+                    const int gamma = warp + PRED_LOAD_WARPS * iss.g;
+                    const int op = gamma < A_GROUPS ? 0 : 1;
+                    const GroupShape gs = group_shape(p, op, op == 0 ? gamma : gamma - A_GROUPS, op == 0 ? 7 : 8,
+                                                      op == 0 ? iss.m0 : iss.n0);
+                    issue_class_group(p, cm, gs, int64_t(iss.kb) * BK, ring + q * GROUP_BYTES, copy_bar(q), lane);
                     iss.next(p, grid);
                     ++issued;
                 }
@@ -811,7 +814,9 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                 const uint32_t q = placed % COPY_DEPTH;
                 if (!mbar_wait(copy_bar(q), (placed / COPY_DEPTH) & 1u, p.wait)) { ok = false; break; }
                 const int gamma = warp + PRED_LOAD_WARPS * fix.g;
-                const GroupShape gs = group_shape(p, gamma, fix.m0, fix.n0);
+                const int op = gamma < A_GROUPS ? 0 : 1;
+                const GroupShape gs = group_shape(p, op, op == 0 ? gamma : gamma - A_GROUPS, op == 0 ? 7 : 8,
+                                                  op == 0 ? fix.m0 : fix.n0);
                 const uint32_t dst = gs.op == 0 ? sA + stage * A_STAGE_BYTES : sB + stage * B_STAGE_BYTES;
                 place_class_group(p, gs, ring + q * GROUP_BYTES, dst, lane);
                 __syncwarp();  // slot q is free for the next copies into it

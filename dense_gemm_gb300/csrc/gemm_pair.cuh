@@ -14,6 +14,13 @@
 //     reuses an accumulator only after both epilogues have released it.
 // Per SM and 64-deep k-block this moves 32 KiB from L2 into shared memory
 // (48 KiB for the single-CTA 128 x 256 tile) for the same tensor work.
+// Predicated-load variant (kTmaLoad = false, operands not describable by one
+// tensor map): four loader warps per CTA each move one 64-line copy group per
+// K-block through the alignment-class tensor maps (see gemm_kernel.cuh). In
+// CTA 0 they arrive on the "full" barrier directly; in CTA 1 on a local
+// "placed" barrier, from which CTA 1's otherwise idle MMA warp relays one
+// cluster-scope arrival to CTA 0 (a release at cluster scope costs a loader
+// warp 1000-3500 cycles; measured with clock64 timestamps).
 #pragma once
 #include "gemm_kernel.cuh"
 
@@ -24,48 +31,67 @@ constexpr int TILE_M = 256;                 // rows per pair tile (128 per CTA)
 constexpr int TILE_N = 256;                 // columns per pair tile (B: 128 per CTA)
 constexpr int CTA_M = 128;
 constexpr int CTA_N = 128;
-constexpr int STAGES = 6;
+constexpr int STAGES = 6;                   // TMA-load variant
 constexpr int A_STAGE_BYTES = CTA_M * BK * 2;  // 16 KiB
 constexpr int B_STAGE_BYTES = CTA_N * BK * 2;  // 16 KiB
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_STAGE_BYTES);
+constexpr int LOAD_WARPS_PRED = 4;          // one copy group (64 lines) each per K-block
+static_assert(LOAD_WARPS_PRED * GROUP_LINES == CTA_M + CTA_N, "loader shares");
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_STAGE_BYTES;
-constexpr int OFF_EPI = OFF_B + STAGES * B_STAGE_BYTES;
-constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-// full[S], empty[S], tfull[2], tempty[2], tdone[2], drain
-constexpr int NUM_BARS = 2 * STAGES + 3 * NUM_ACC + 1;
-constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_USED = OFF_TMEM_SLOT + 16;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;
-constexpr int THREADS = (1 + 1 + EPI_WARPS) * 32;
-
-static_assert(OFF_B % 1024 == 0 && OFF_EPI % 1024 == 0, "swizzled buffers need 1 KiB alignment");
-static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+// Shared-memory map. The predicated-load variant keeps two operand stages and
+// holds the loader warps' staging rings (one mbarrier per slot) instead.
+template <bool kTmaLoad>
+struct Layout {
+    static constexpr int stages = kTmaLoad ? STAGES : 2;
+    static constexpr int load_warps = kTmaLoad ? 1 : LOAD_WARPS_PRED;
+    static constexpr int threads = (load_warps + 1 + EPI_WARPS) * 32;
+    static constexpr int off_a = 0;
+    static constexpr int off_b = off_a + stages * A_STAGE_BYTES;
+    static constexpr int off_epi = off_b + stages * B_STAGE_BYTES;
+    static constexpr int off_copy = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+    static constexpr int copy_slots = kTmaLoad ? 0 : LOAD_WARPS_PRED * COPY_DEPTH;
+    static constexpr int off_bar = off_copy + copy_slots * GROUP_BYTES;
+    // full[S], empty[S], tfull[2], tempty[2], tdone[2], drain, then for predicated
+    // loads placed[S] (CTA 1's loaders -> its relay) and the copy-slot barriers
+    static constexpr int placed_bar0 = 2 * stages + 3 * NUM_ACC + 1;
+    static constexpr int copy_bar0 = placed_bar0 + (kTmaLoad ? 0 : stages);
+    static constexpr int num_bars = copy_bar0 + copy_slots;
+    static constexpr int off_tmem_slot = off_bar + num_bars * 8;
+    static constexpr int smem_bytes = off_tmem_slot + 16 + 1024;
+    static_assert(off_b % 1024 == 0 && off_epi % 1024 == 0, "swizzled buffers need 1 KiB alignment");
+    static_assert(off_copy % 128 == 0, "TMA box destinations need 128-byte alignment");
+    static_assert(smem_bytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
+};
+constexpr int SMEM_BYTES = Layout<true>::smem_bytes;
+constexpr int THREADS = Layout<true>::threads;
 }  // namespace pair
 
-template <bool kTmaStore>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
+template <bool kTmaLoad, bool kTmaStore>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoad>::threads, 1)
     gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmC, const Params p) {
-    constexpr int MMA_WARP = 1;
-    constexpr int EPI_WARP0 = 2;
+                  const __grid_constant__ CUtensorMap tmC, const Params p,
+                  const __grid_constant__ typename ClassMapsFor<kTmaLoad>::type cm) {
+    using Lay = pair::Layout<kTmaLoad>;
+    constexpr int NST = Lay::stages;
+    constexpr int LOAD_WARPS = Lay::load_warps;
+    constexpr int MMA_WARP = LOAD_WARPS;
+    constexpr int EPI_WARP0 = LOAD_WARPS + 1;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // same offset in both CTAs
     uint8_t *smem = smem_raw + (base - raw);
 
-    const uint32_t sA = base + pair::OFF_A;
-    const uint32_t sB = base + pair::OFF_B;
-    const uint32_t bar0 = base + pair::OFF_BAR;
+    const uint32_t sA = base + Lay::off_a;
+    const uint32_t sB = base + Lay::off_b;
+    const uint32_t bar0 = base + Lay::off_bar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (pair::STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * pair::STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * pair::STAGES + NUM_ACC + a); };
-    auto tdone_bar = [&](int a) { return bar0 + 8u * (2 * pair::STAGES + 2 * NUM_ACC + a); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * pair::STAGES + 3 * NUM_ACC);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + pair::OFF_TMEM_SLOT);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (NST + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NST + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NST + NUM_ACC + a); };
+    auto tdone_bar = [&](int a) { return bar0 + 8u * (2 * NST + 2 * NUM_ACC + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * NST + 3 * NUM_ACC);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::off_tmem_slot);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -74,8 +100,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     const int32_t num_pairs = int32_t(gridDim.x >> 1);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < pair::STAGES; ++s) {
-            mbar_init(full_bar(s), 1);   // CTA 0's arrive.expect_tx; both CTAs' bytes
+        for (int s = 0; s < NST; ++s) {
+            // TMA loads: CTA 0's arrive.expect_tx, both CTAs' bytes; predicated
+            // loads: CTA 0's loader warps plus CTA 1's relay
+            mbar_init(full_bar(s), kTmaLoad ? 1 : LOAD_WARPS + 1);
             mbar_init(empty_bar(s), 1);  // CTA 0's MMA commit (multicast)
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -84,15 +112,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
             mbar_init(tdone_bar(a), EPI_WARPS);       // this CTA's epilogue warps
         }
         mbar_init(drain_bar, 1);
+        if (!kTmaLoad)
+            for (int q = 0; q < NST; ++q) mbar_init(bar0 + 8u * (Lay::placed_bar0 + q), LOAD_WARPS);
+        for (int q = 0; q < Lay::copy_slots; ++q) mbar_init(bar0 + 8u * (Lay::copy_bar0 + q), 1);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {  // one warp in each CTA of the pair, collectively
         tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
         tmem_relinquish_pair();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+    if constexpr (kTmaLoad) {
+        if (warp == 0 && lane == 0) {
+            prefetch_tensormap(&tmA);
+            prefetch_tensormap(&tmB);
+        }
+    } else {
+        if (warp == 0 && lane < 2 * MAX_CLASSES) {  // the maps of classes that hold rows
+            const int op = lane / MAX_CLASSES, cls = lane % MAX_CLASSES;
+            if ((p.cls_live[op] >> cls) & 1u) prefetch_tensormap(op == 0 ? &cm.a[cls] : &cm.b[cls]);
+        }
     }
     if (kTmaStore && warp == EPI_WARP0 && lane == 0) prefetch_tensormap(&tmC);
     tc_fence_before();
@@ -101,7 +139,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int32_t num_kb = p.num_kb;
 
-    if (warp == 0) {
+    if (!kTmaLoad && warp < LOAD_WARPS) {
+        // ============================================================ predicated loaders (both CTAs)
+        // Warp w moves copy group w & 1 of operand w >> 1 (this CTA's 128 rows of
+        // A, or 128 columns of B) for every K-block, through a COPY_DEPTH-slot
+        // staging ring; lane 0 keeps the TMA copies of later K-blocks in flight.
+        // With cross-tile off, copies stop at each unit boundary until this
+        // CTA's epilogue has drained the previous unit.
+        if constexpr (!kTmaLoad) {
+            const uint32_t ring = base + Lay::off_copy + uint32_t(warp) * (COPY_DEPTH * GROUP_BYTES);
+            auto copy_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::copy_bar0 + warp * COPY_DEPTH + q); };
+            const int op = warp >> 1, grp = warp & 1;
+            struct Cursor {
+                int32_t u, it, kb, kb0, kb1;
+                int64_t mn0;
+            };
+            auto setup = [&](Cursor &c) {
+                if (c.u >= p.num_units) return;
+                const int32_t tile = c.u % p.num_tiles, split = c.u / p.num_tiles;
+                c.kb0 = split * p.kb_per_split;
+                c.kb1 = min(num_kb, c.kb0 + p.kb_per_split);
+                c.kb = c.kb0;
+                int32_t tm, tn;
+                tile_coords(tile, p.sched, tm, tn);
+                c.mn0 = op == 0 ? int64_t(tm) * pair::TILE_M + int64_t(rank) * pair::CTA_M
+                                : int64_t(tn) * pair::TILE_N + int64_t(rank) * pair::CTA_N;
+            };
+            auto advance = [&](Cursor &c) {
+                if (++c.kb < c.kb1) return;
+                c.u += num_pairs;
+                ++c.it;
+                setup(c);
+            };
+            Cursor iss{pair_id, 0, 0, 0, 0, 0};
+            setup(iss);
+            Cursor fix = iss;
+            uint32_t issued = 0, placed = 0, stage = 0, phase = 0;
+            bool ok = true;
+            // CTA 0 signals its own full barrier, CTA 1 its placed barrier (relayed)
+            const uint32_t done0 = rank == 0 ? full_bar(0) : bar0 + 8u * Lay::placed_bar0;
+            while (fix.u < p.num_units) {
+                if (fix.kb == fix.kb0 && !p.cross_tile && fix.it > 0) {
+                    const int32_t j = fix.it - 1;  // this CTA's epilogue has drained unit j
+                    if (!mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
+                }
+                while (issued - placed < COPY_DEPTH && iss.u < p.num_units && (p.cross_tile || iss.it == fix.it)) {
+                    const uint32_t q = issued % COPY_DEPTH;
+                    const GroupShape gs = group_shape(p, op, grp, 7, iss.mn0);
+                    issue_class_group(p, cm, gs, int64_t(iss.kb) * BK, ring + q * GROUP_BYTES, copy_bar(q), lane);
+                    advance(iss);
+                    ++issued;
+                }
+                if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
+                const uint32_t q = placed % COPY_DEPTH;
+                if (!mbar_wait(copy_bar(q), (placed / COPY_DEPTH) & 1u, p.wait)) { ok = false; break; }
+                const GroupShape gs = group_shape(p, op, grp, 7, fix.mn0);
+                place_class_group(p, gs, ring + q * GROUP_BYTES,
+                                  op == 0 ? sA + stage * pair::A_STAGE_BYTES : sB + stage * pair::B_STAGE_BYTES,
+                                  lane);
+                fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(done0 + 8u * stage);
+                if (++stage == NST) { stage = 0; phase ^= 1u; }
+                advance(fix);
+                ++placed;
+            }
+            if (!ok) {
+                // Let the copies this warp started land before the CTA exits.
+                for (uint32_t q = placed; q < issued; ++q)
+                    mbar_wait_slow(copy_bar(q % COPY_DEPTH), (q / COPY_DEPTH) & 1u, cleanup_wait(p.wait), false);
+            }
+        }
+    } else if (warp == 0) {
         // ============================================================ producer (both CTAs)
         if (lane == 0) {
             const uint64_t pol_ld = l2_policy_evict_last();
@@ -161,15 +270,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                         }
                     }
                     ++issued;
-                    if (++stage == pair::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
                 }
             }
             if (!ok) {
                 if (rank == 0) {
                     // Let the copies counted on this CTA's barriers land before exiting.
-                    const uint32_t n = issued < pair::STAGES ? issued : pair::STAGES;
+                    const uint32_t n = issued < NST ? issued : NST;
                     for (uint32_t q = issued - n; q < issued; ++q)
-                        mbar_wait_slow(full_bar(q % pair::STAGES), (q / pair::STAGES) & 1u,
+                        mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u,
                                        cleanup_wait(p.wait), false);
                 } else {
                     // The peer's copies count on CTA 0's barriers, which it cannot
@@ -183,6 +292,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
+        if (!kTmaLoad && rank == 1) {
+            // ======================================================== relay (CTA 1, predicated loads)
+            // Once this CTA's loader warps have filled a stage, one release at
+            // cluster scope hands it to CTA 0's full barrier.
+            uint32_t stage = 0, phase = 0;
+            const uint32_t full0 = mapa_shared(full_bar(0), 0);
+            for (int32_t u = pair_id; u < p.num_units; u += num_pairs) {
+                const int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
+                const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+                bool ok = true;
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(bar0 + 8u * (Lay::placed_bar0 + stage), phase, p.wait))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) mbar_arrive_cluster(full0 + 8u * stage);
+                    __syncwarp();
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+            }
+        }
         // ============================================================ MMA issuer (CTA 0)
         // Whole warp, warp-uniform values; one elected lane issues (see the
         // single-CTA kernel).
@@ -206,7 +338,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * pair::TILE_N;
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(full_bar(stage), phase, p.wait))) {
+                    // predicated loads: arrivals from the peer CTA's loader warps,
+                    // acquired at cluster scope
+                    const bool full = kTmaLoad ? mbar_wait(full_bar(stage), phase, p.wait)
+                                               : mbar_wait_cluster(full_bar(stage), phase, p.wait);
+                    if (!__all_sync(0xffffffffu, full)) {
                         ok = false;
                         break;
                     }
@@ -218,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
                         mma_f16_pair_elect(d_tmem, a0 + k16 * da.k16, b0 + k16 * db.k16, idesc,
                                            ((kb - kb0) | k16) != 0 ? 1u : 0u);
                     mma_commit_pair_mc_elect(empty_bar(stage), 0x3);  // both CTAs' slots reusable
-                    if (++stage == pair::STAGES) { stage = 0; phase ^= 1u; }
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
                 mma_commit_pair_mc_elect(tfull_bar(acc), 0x3);  // both halves of the tile complete
@@ -231,7 +367,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::THREADS, 1)
         const int q = warp & 3;
         const int ew = warp - EPI_WARP0;
         const int half = ew / 4;
-        const uint32_t stg = base + pair::OFF_EPI + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
+        const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         int32_t it = 0;
         for (int32_t u = pair_id; u < p.num_units; u += num_pairs, ++it) {
             const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;

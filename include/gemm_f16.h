@@ -89,11 +89,11 @@ typedef enum {
  * boundary below each row start: it may read, and discard, bytes that share
  * an aligned 16-byte granule with an element of A or B, never others. If the
  * driver rejects such a class description -> GEMM_ERR_UNSUPPORTED.
- * With TMA-loadable A and B the work is split into 256x256 output
- * tiles, each computed by a pair of CTAs on the two SMs of a TPC (tcgen05
- * cta_group::2); otherwise, or with GEMM_SCHED_SINGLE_CTA, into 128x256 tiles
- * of one CTA each. The tile order (row-major / grouped) applies to whichever
- * tiles are used; a "program" of the persistent order is a CTA pair or a CTA.
+ * The work is split into 256x256 output tiles, each computed by a pair of
+ * CTAs on the two SMs of a TPC (tcgen05 cta_group::2), or with
+ * GEMM_SCHED_SINGLE_CTA into 128x256 tiles of one CTA each. The tile order
+ * (row-major / grouped) applies to whichever tiles are used; a "program" of
+ * the persistent order is a CTA pair or a CTA.
  * GEMM_SCHED_NON_PERSISTENT launches one program per tile ([persistent]
  * "naive tiled matmul" grid); program p then computes tile_id p only, and
  * GEMM_SCHED_CROSS_TILE has nothing to overlap.
@@ -236,8 +236,8 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags,
  * gemm_f16_kernel_info — compiled resource use of a kernel variant
  * (cudaFuncGetAttributes). One-CTA tiles: variant 0 = TMA loads + TMA store,
  * 1 = TMA loads + predicated store, 2 = predicated loads + TMA store,
- * 3 = predicated loads + predicated store. CTA-pair tiles: 4 = TMA store,
- * 5 = predicated store. Outputs may be NULL. Needs a device.
+ * 3 = predicated loads + predicated store. CTA-pair tiles, in the same
+ * order: 4, 5, 6, 7. Outputs may be NULL. Needs a device.
  */
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *static_smem, int32_t *dynamic_smem,
