@@ -406,6 +406,33 @@ __device__ __forceinline__ void issue_class_group(const Params &p, const ClassMa
     }
 }
 
+// Issues the TMA copies of one group from the calling lane: `bi` is the box
+// index within the group; box 0's lane announces the group's byte count on
+// `bar` first (ordered before the other boxes' issue by the caller's warp
+// convergence through __syncwarp). Boxes of classes without rows are skipped.
+__device__ __forceinline__ void issue_class_group_lanes(const Params &p, const ClassMaps &cm,
+                                                        const GroupShape &gs, int64_t k0, uint32_t slot,
+                                                        uint32_t bar, int bi) {
+    const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
+    const int nbox = GROUP_LINES >> gs.lh;
+    const uint32_t box_bytes = uint32_t(LINE_PITCH) << gs.lh;
+    if (bi == 0) {
+        uint32_t boxes = 0;
+        for (int i = 0; i < nbox; ++i) boxes += (live >> gs.cls(gs.first_box + i)) & 1u;
+        mbar_arrive_expect_tx(bar, boxes * box_bytes);
+    }
+    __syncwarp();
+    if (bi < nbox) {
+        const int32_t xb = int32_t(gs.mn_major ? gs.mn0 : k0);
+        const int32_t yb = int32_t((gs.mn_major ? k0 : gs.mn0) >> gs.lp);
+        const int beta = gs.first_box + bi, cls = gs.cls(beta);
+        const CUtensorMap *maps = gs.op == 0 ? cm.a : cm.b;
+        if ((live >> cls) & 1u)
+            tma_load_2d(slot + uint32_t(bi) * box_bytes, &maps[cls], xb + 64 * gs.seg(beta),
+                        yb + (gs.blk(beta) << gs.lh), bar);
+    }
+}
+
 // Bytes [m, m + 16) of the 32-byte window w[0..7] (m even, 0..14): select
 // by whole words (m / 4), then shift by a half word when m % 4 == 2.
 __device__ __forceinline__ void window16(const uint32_t (&w)[8], uint32_t m, uint32_t (&o)[4]) {

@@ -15,9 +15,12 @@
 // Per SM and 64-deep k-block this moves 32 KiB from L2 into shared memory
 // (48 KiB for the single-CTA 128 x 256 tile) for the same tensor work.
 // Predicated-load variant (kTmaLoad = false, operands not describable by one
-// tensor map): four loader warps per CTA each move one 64-line copy group per
-// K-block through the alignment-class tensor maps (see gemm_kernel.cuh). In
-// CTA 0 they arrive on the "full" barrier directly; in CTA 1 on a local
+// tensor map): per CTA one warp issues the TMA copies of the alignment-class
+// boxes (see gemm_kernel.cuh) into four staging rings, and four warps each
+// shift one 64-line copy group per K-block into the stage (a TMA issue stalls
+// its warp ~110-175 cycles, so issuing apart from the shifting overlaps the
+// two). In CTA 0 the shifting warps arrive on the "full" barrier directly; in
+// CTA 1 on a local
 // "placed" barrier, from which CTA 1's otherwise idle MMA warp relays one
 // cluster-scope arrival to CTA 0 (a release at cluster scope costs a loader
 // warp 1000-3500 cycles; measured with clock64 timestamps).
@@ -35,27 +38,31 @@ constexpr int STAGES = 6;                   // TMA-load variant
 constexpr int A_STAGE_BYTES = CTA_M * BK * 2;  // 16 KiB
 constexpr int B_STAGE_BYTES = CTA_N * BK * 2;  // 16 KiB
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_STAGE_BYTES);
-constexpr int LOAD_WARPS_PRED = 4;          // one copy group (64 lines) each per K-block
-static_assert(LOAD_WARPS_PRED * GROUP_LINES == CTA_M + CTA_N, "loader shares");
+constexpr int PLACE_WARPS = 4;              // predicated loads: one copy group (64 lines) each per K-block
+static_assert(PLACE_WARPS * GROUP_LINES == CTA_M + CTA_N, "loader shares");
 
 // Shared-memory map. The predicated-load variant keeps two operand stages and
 // holds the loader warps' staging rings (one mbarrier per slot) instead.
 template <bool kTmaLoad>
 struct Layout {
     static constexpr int stages = kTmaLoad ? STAGES : 2;
-    static constexpr int load_warps = kTmaLoad ? 1 : LOAD_WARPS_PRED;
+    // TMA loads: one producer warp. Predicated loads: PLACE_WARPS warps that
+    // shift staged lines into the stages, then one warp that issues their copies.
+    static constexpr int load_warps = kTmaLoad ? 1 : PLACE_WARPS + 1;
     static constexpr int threads = (load_warps + 1 + EPI_WARPS) * 32;
     static constexpr int off_a = 0;
     static constexpr int off_b = off_a + stages * A_STAGE_BYTES;
     static constexpr int off_epi = off_b + stages * B_STAGE_BYTES;
     static constexpr int off_copy = off_epi + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-    static constexpr int copy_slots = kTmaLoad ? 0 : LOAD_WARPS_PRED * COPY_DEPTH;
+    static constexpr int copy_slots = kTmaLoad ? 0 : PLACE_WARPS * COPY_DEPTH;
     static constexpr int off_bar = off_copy + copy_slots * GROUP_BYTES;
     // full[S], empty[S], tfull[2], tempty[2], tdone[2], drain, then for predicated
-    // loads placed[S] (CTA 1's loaders -> its relay) and the copy-slot barriers
+    // loads placed[S] (CTA 1's loaders -> its relay), the copy-slot barriers
+    // (copies landed) and slot_free[COPY_DEPTH] (slot read by every placing warp)
     static constexpr int placed_bar0 = 2 * stages + 3 * NUM_ACC + 1;
     static constexpr int copy_bar0 = placed_bar0 + (kTmaLoad ? 0 : stages);
-    static constexpr int num_bars = copy_bar0 + copy_slots;
+    static constexpr int free_bar0 = copy_bar0 + copy_slots;
+    static constexpr int num_bars = free_bar0 + (kTmaLoad ? 0 : COPY_DEPTH);
     static constexpr int off_tmem_slot = off_bar + num_bars * 8;
     static constexpr int smem_bytes = off_tmem_slot + 16 + 1024;
     static_assert(off_b % 1024 == 0 && off_epi % 1024 == 0, "swizzled buffers need 1 KiB alignment");
@@ -102,8 +109,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             // TMA loads: CTA 0's arrive.expect_tx, both CTAs' bytes; predicated
-            // loads: CTA 0's loader warps plus CTA 1's relay
-            mbar_init(full_bar(s), kTmaLoad ? 1 : LOAD_WARPS + 1);
+            // loads: CTA 0's shifting warps plus CTA 1's relay
+            mbar_init(full_bar(s), kTmaLoad ? 1 : pair::PLACE_WARPS + 1);
             mbar_init(empty_bar(s), 1);  // CTA 0's MMA commit (multicast)
         }
         for (int a = 0; a < NUM_ACC; ++a) {
@@ -112,8 +119,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             mbar_init(tdone_bar(a), EPI_WARPS);       // this CTA's epilogue warps
         }
         mbar_init(drain_bar, 1);
-        if (!kTmaLoad)
-            for (int q = 0; q < NST; ++q) mbar_init(bar0 + 8u * (Lay::placed_bar0 + q), LOAD_WARPS);
+        if (!kTmaLoad) {
+            for (int q = 0; q < NST; ++q) mbar_init(bar0 + 8u * (Lay::placed_bar0 + q), pair::PLACE_WARPS);
+            for (int q = 0; q < COPY_DEPTH; ++q) mbar_init(bar0 + 8u * (Lay::free_bar0 + q), pair::PLACE_WARPS);
+        }
         for (int q = 0; q < Lay::copy_slots; ++q) mbar_init(bar0 + 8u * (Lay::copy_bar0 + q), 1);
         fence_mbar_init();
     }
@@ -140,19 +149,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     const int32_t num_kb = p.num_kb;
 
     if (!kTmaLoad && warp < LOAD_WARPS) {
-        // ============================================================ predicated loaders (both CTAs)
-        // Warp w moves copy group w & 1 of operand w >> 1 (this CTA's 128 rows of
-        // A, or 128 columns of B) for every K-block, through a COPY_DEPTH-slot
-        // staging ring; lane 0 keeps the TMA copies of later K-blocks in flight.
-        // With cross-tile off, copies stop at each unit boundary until this
-        // CTA's epilogue has drained the previous unit.
+        // ============================================================ predicated loads (both CTAs)
+        // Warp w < PLACE_WARPS shifts copy group w & 1 of operand w >> 1 (this
+        // CTA's 128 rows of A, or 128 columns of B) for every K-block out of its
+        // COPY_DEPTH-slot staging ring; warp PLACE_WARPS issues the copies, up to
+        // COPY_DEPTH K-blocks ahead. With cross-tile off the copies of a unit
+        // start only after this CTA's epilogue has drained the previous unit.
         if constexpr (!kTmaLoad) {
-            const uint32_t ring = base + Lay::off_copy + uint32_t(warp) * (COPY_DEPTH * GROUP_BYTES);
-            auto copy_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::copy_bar0 + warp * COPY_DEPTH + q); };
-            const int op = warp >> 1, grp = warp & 1;
+            constexpr int PW = pair::PLACE_WARPS;
+            auto ring = [&](int w) { return base + Lay::off_copy + uint32_t(w) * (COPY_DEPTH * GROUP_BYTES); };
+            auto copy_bar = [&](int w, uint32_t q) { return bar0 + 8u * (Lay::copy_bar0 + w * COPY_DEPTH + q); };
+            auto free_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::free_bar0 + q); };
             struct Cursor {
                 int32_t u, it, kb, kb0, kb1;
-                int64_t mn0;
+                int64_t m0, n0;  // this CTA's first row of A and column of B
             };
             auto setup = [&](Cursor &c) {
                 if (c.u >= p.num_units) return;
@@ -162,8 +172,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 c.kb = c.kb0;
                 int32_t tm, tn;
                 tile_coords(tile, p.sched, tm, tn);
-                c.mn0 = op == 0 ? int64_t(tm) * pair::TILE_M + int64_t(rank) * pair::CTA_M
-                                : int64_t(tn) * pair::TILE_N + int64_t(rank) * pair::CTA_N;
+                c.m0 = int64_t(tm) * pair::TILE_M + int64_t(rank) * pair::CTA_M;
+                c.n0 = int64_t(tn) * pair::TILE_N + int64_t(rank) * pair::CTA_N;
             };
             auto advance = [&](Cursor &c) {
                 if (++c.kb < c.kb1) return;
@@ -171,43 +181,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 ++c.it;
                 setup(c);
             };
-            Cursor iss{pair_id, 0, 0, 0, 0, 0};
-            setup(iss);
-            Cursor fix = iss;
-            uint32_t issued = 0, placed = 0, stage = 0, phase = 0;
+            Cursor c{pair_id, 0, 0, 0, 0, 0, 0};
+            setup(c);
+            uint32_t n = 0;  // K-blocks handled so far
             bool ok = true;
-            // CTA 0 signals its own full barrier, CTA 1 its placed barrier (relayed)
-            const uint32_t done0 = rank == 0 ? full_bar(0) : bar0 + 8u * Lay::placed_bar0;
-            while (fix.u < p.num_units) {
-                if (fix.kb == fix.kb0 && !p.cross_tile && fix.it > 0) {
-                    const int32_t j = fix.it - 1;  // this CTA's epilogue has drained unit j
-                    if (!mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
+            if (warp == PW) {
+                // ---- copy issuer: lane 8w + i issues box i of shifting warp w's group
+                const int w = lane >> 3, bi = lane & 7;
+                for (; c.u < p.num_units; advance(c), ++n) {
+                    if (c.kb == c.kb0 && !p.cross_tile && c.it > 0) {
+                        const int32_t j = c.it - 1;  // this CTA's epilogue has drained unit j
+                        if (!__all_sync(0xffffffffu, mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait))) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const uint32_t q = n % COPY_DEPTH;
+                    // every shifting warp has read the slot's previous contents
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(free_bar(q), ((n / COPY_DEPTH) & 1u) ^ 1u, p.wait))) {
+                        ok = false;
+                        break;
+                    }
+                    const int op = w >> 1;
+                    const GroupShape gs = group_shape(p, op, w & 1, 7, op == 0 ? c.m0 : c.n0);
+                    issue_class_group_lanes(p, cm, gs, int64_t(c.kb) * BK, ring(w) + q * GROUP_BYTES,
+                                            copy_bar(w, q), bi);
                 }
-                while (issued - placed < COPY_DEPTH && iss.u < p.num_units && (p.cross_tile || iss.it == fix.it)) {
-                    const uint32_t q = issued % COPY_DEPTH;
-                    const GroupShape gs = group_shape(p, op, grp, 7, iss.mn0);
-                    issue_class_group(p, cm, gs, int64_t(iss.kb) * BK, ring + q * GROUP_BYTES, copy_bar(q), lane);
-                    advance(iss);
-                    ++issued;
+                if (!ok) {
+                    // Let the copies this warp started land before the CTA exits.
+                    const uint32_t first = n > COPY_DEPTH ? n - COPY_DEPTH : 0;
+                    for (uint32_t m = first; m < n; ++m)
+                        for (int w2 = 0; w2 < PW; ++w2)
+                            mbar_wait_slow(copy_bar(w2, m % COPY_DEPTH), (m / COPY_DEPTH) & 1u,
+                                           cleanup_wait(p.wait), false);
                 }
-                if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
-                const uint32_t q = placed % COPY_DEPTH;
-                if (!mbar_wait(copy_bar(q), (placed / COPY_DEPTH) & 1u, p.wait)) { ok = false; break; }
-                const GroupShape gs = group_shape(p, op, grp, 7, fix.mn0);
-                place_class_group(p, gs, ring + q * GROUP_BYTES,
-                                  op == 0 ? sA + stage * pair::A_STAGE_BYTES : sB + stage * pair::B_STAGE_BYTES,
-                                  lane);
-                fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
-                __syncwarp();
-                if (lane == 0) mbar_arrive(done0 + 8u * stage);
-                if (++stage == NST) { stage = 0; phase ^= 1u; }
-                advance(fix);
-                ++placed;
-            }
-            if (!ok) {
-                // Let the copies this warp started land before the CTA exits.
-                for (uint32_t q = placed; q < issued; ++q)
-                    mbar_wait_slow(copy_bar(q % COPY_DEPTH), (q / COPY_DEPTH) & 1u, cleanup_wait(p.wait), false);
+            } else {
+                // ---- shifting warp
+                const int op = warp >> 1, grp = warp & 1;
+                uint32_t stage = 0, phase = 0;
+                // CTA 0 signals its own full barrier, CTA 1 its placed barrier (relayed)
+                const uint32_t done0 = rank == 0 ? full_bar(0) : bar0 + 8u * Lay::placed_bar0;
+                for (; c.u < p.num_units; advance(c), ++n) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) break;
+                    const uint32_t q = n % COPY_DEPTH;
+                    if (!mbar_wait(copy_bar(warp, q), (n / COPY_DEPTH) & 1u, p.wait)) break;
+                    const GroupShape gs = group_shape(p, op, grp, 7, op == 0 ? c.m0 : c.n0);
+                    place_class_group(p, gs, ring(warp) + q * GROUP_BYTES,
+                                      op == 0 ? sA + stage * pair::A_STAGE_BYTES : sB + stage * pair::B_STAGE_BYTES,
+                                      lane);
+                    // generic-proxy writes -> visible to the tensor core; this
+                    // warp's staging reads ordered before the slot's next copies
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(done0 + 8u * stage);
+                        mbar_arrive(free_bar(q));
+                    }
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
+                }
             }
         }
     } else if (warp == 0) {
