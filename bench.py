@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -213,6 +214,20 @@ def oracle_rows_timing(A, B, rows, threads):
     return time.perf_counter() - t0
 
 
+def host_cpu():
+    """CPU model and architecture of this host (for the CPU-baseline line)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"model": model or platform.processor() or "unknown", "machine": platform.machine()}
+
+
 def cpu_baseline(A, B, seconds):
     """Time the oracle, as it stands, on a bounded sample of whole C rows."""
     import numpy as np
@@ -228,7 +243,7 @@ def cpu_baseline(A, B, seconds):
     t = oracle_rows_timing(A, B, sample, threads)
     flops = 2.0 * rows * N * K
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": int(oracle.max_threads()),
-            "kind": "oracle",
+            "kind": "oracle", "host": host_cpu(),
             "sample": f"{rows} random rows of C (full N={N}, K={K}) = {rows / M:.4%} of the "
                       f"workload's FLOPs, {t:.1f} s on {threads} host threads"}
 
@@ -261,7 +276,7 @@ def run_reference(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w, args, {"rows_per_step": rows}),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "kind": "oracle",
-                         "cores": int(oracle.max_threads()),
+                         "cores": int(oracle.max_threads()), "host": host_cpu(),
                          "sample": f"each step: {rows} random whole rows of C "
                                    f"({rows / M:.4%} of the workload)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -302,6 +317,17 @@ def run_gpu(args, w):
     torch.cuda.synchronize(dev)
     if sync_status(stream) != 0:
         raise RuntimeError("device status after warm-up is not GEMM_OK")
+
+    # one launch right after a 512 MiB write has flushed L2, next to the warm loop below
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush.fill_(1)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    step()
+    c1.record(stream)
+    torch.cuda.synchronize(dev)
+    cold_l2_ms = c0.elapsed_time(c1)
+    del flush
 
     sampler = None
     if not args.no_clocks:
@@ -406,13 +432,14 @@ def run_gpu(args, w):
                      "frac_of_sustained_peak": (achieved / sustained) if sustained else None,
                      "sustained_peak": sustained,
                      "kernel": ("g16::gemm_f16_persistent<true,true>" if args.single_cta
-                                else "g16::gemm_f16_pair<true>"),
+                                else "g16::gemm_f16_pair<true,true>"),
                      "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": avg_launch_ms, "median_launch_ms": med_launch_ms,
                      "workload_roofline_tflops_min_P_BWxI": bound_tflops,
                      "compulsory_bytes": compulsory},
         "e2e": e2e,
         "gpu_launches": K_steps,
+        "cold_l2_launch_ms": cold_l2_ms,
         "clocks": clocks,
         "kernel_resources": info,
         "device_status": status,
