@@ -228,6 +228,33 @@ def host_cpu():
     return {"model": model or platform.processor() or "unknown", "machine": platform.machine()}
 
 
+def host_link_rates(h2d_bytes, d2h_bytes, dev, reps=3):
+    """GB/s of one pinned-host <-> device copy of each size (best of `reps`)."""
+    import torch
+    host_in = torch.empty(h2d_bytes, dtype=torch.uint8, pin_memory=True)
+    host_out = torch.empty(d2h_bytes, dtype=torch.uint8, pin_memory=True)
+    dev_in = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dev_out = torch.zeros(d2h_bytes, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(dev)
+
+    def best(fn, nbytes):
+        t = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            with torch.cuda.stream(s):
+                fn()
+            e1.record(s)
+            s.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return nbytes / (min(t) * 1e-3) / 1e9
+
+    rates = {"h2d": best(lambda: dev_in.copy_(host_in, non_blocking=True), h2d_bytes),
+             "d2h": best(lambda: host_out.copy_(dev_out, non_blocking=True), d2h_bytes)}
+    del host_in, host_out, dev_in, dev_out
+    return rates
+
+
 def cpu_baseline(A, B, seconds):
     """Time the oracle, as it stands, on a bounded sample of whole C rows."""
     import numpy as np
@@ -375,6 +402,9 @@ def run_gpu(args, w):
         C_pin = torch.empty((w.M, w.N), dtype=torch.float32, pin_memory=True)
         del C  # the pipeline holds its own device buffers
         torch.cuda.empty_cache()
+        in_bytes = A_host.untyped_storage().nbytes() + B_host.untyped_storage().nbytes()
+        out_bytes = 4 * w.M * w.N
+        link = host_link_rates(in_bytes, out_bytes, dev)
         pipe = HostPipeline(A, B, depth=2, group_size_m=args.group_size, grouped=grouped,
                             cross_tile=cross, single_cta=args.single_cta, device=dev)
         del A, B
@@ -390,9 +420,11 @@ def run_gpu(args, w):
         e1.record(pipe.s_out)
         pipe.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-        in_bytes = A_host.untyped_storage().nbytes() + B_host.untyped_storage().nbytes()
         e2e = {"value": job_throughput(world, flops, args.e2e_steps, e2e_ms), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": 4 * w.M * w.N,
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
+               "link_gbs": link,
+               # uploads and downloads of consecutive steps overlap: the slower direction bounds a step
+               "link_bound_ms_per_step": max(in_bytes / link["h2d"], out_bytes / link["d2h"]) / 1e6,
                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
                "api": "dense_gemm_gb300.HostPipeline (pinned host A, B -> device, gemm_f16, "
                       "C -> pinned host; upload+GEMM of step i+1 overlap the download of step i)"}

@@ -620,8 +620,13 @@ gemm_status_t gemm_f16_sync_status(gemm_stream_t stream_) {
     unsigned int st = 0;
     const unsigned int zero = 0;
     if (cudaMemcpyFromSymbol(&st, g_status, sizeof(st)) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (st != 0 && cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess)
-        return GEMM_ERR_CUDA;
+    if (st != 0) {
+        // clear the status, and the aborted launch's epoch: a CUDA graph replays a
+        // launch with the epoch it was captured with
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess ||
+            cudaMemcpyToSymbol(g_abort_epoch, &zero, sizeof(zero)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
     return st == 0 ? GEMM_OK : static_cast<gemm_status_t>(st);
 }
 

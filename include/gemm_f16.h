@@ -248,6 +248,10 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
  * sticky device status of the current device: GEMM_ERR_TIMEOUT if any
  * kernel's bounded wait ran out since the last call (that call's C is
  * undefined), GEMM_ERR_CUDA if the synchronize failed, else GEMM_OK.
+ * Calls of the other entry points enqueue work only (no synchronisation, no
+ * allocation after the first call on a device), so they can be captured in a
+ * CUDA graph; a replayed launch reuses its captured abort epoch, which this
+ * call clears together with the status.
  */
 gemm_status_t gemm_f16_sync_status(gemm_stream_t stream);
 

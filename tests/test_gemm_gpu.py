@@ -249,6 +249,39 @@ def test_repeated_calls_and_streams():
         assert np.array_equal(o.cpu().numpy().astype(np.float64), ref)
 
 
+def test_calls_captured_in_a_cuda_graph():
+    """The entry points only enqueue work (no host synchronisation, no
+    allocation), so calls can be captured into a CUDA graph and replayed:
+    TMA and predicated paths, fp32 and 16-bit outputs."""
+    A = draw(700, 520, "int", 93)
+    B = draw(520, 900, "int", 94)
+    ref = oracle.gemm(A, B)
+    Ad, Bd = to_dev(A), to_dev(B)
+    Au = to_dev(relayout(A, "row", pad=3, offset=1))  # predicated loads
+    outs = [torch.full((700, 900), float("nan"), device="cuda") for _ in range(2)]
+    out16 = torch.full((700, 900), float("nan"), device="cuda", dtype=torch.float16)
+    for o, a in zip(outs, (Ad, Au)):  # first calls (library set-up) outside the capture
+        gemm(a, Bd, o)
+    gemm(Ad, Bd, out16)
+    torch.cuda.synchronize()
+    for o in outs + [out16]:
+        o.fill_(float("nan"))
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        gemm(Ad, Bd, outs[0])
+        gemm(Au, Bd, outs[1])
+        gemm(Ad, Bd, out16)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert sync_status() == 0
+    for o in outs:
+        assert np.array_equal(o.cpu().numpy().astype(np.float64), ref)
+    np.testing.assert_array_equal(out16.cpu().numpy().astype(np.float64),
+                                  oracle.round_output(ref, "f16"))
+
+
 # ------------------------------------------------------------------ full workload sizes
 
 def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=False):
