@@ -497,8 +497,9 @@ __device__ __forceinline__ void place_class_group(const Params &p, const GroupSh
 // the chunks are spread over the next unit's main loop (the accumulator is only
 // needed again two units later). Measured at 16384^2 x 4096: tensor-pipe
 // activity 89 % -> 92 %.
-// Without cross-tile overlap the producer waits for the epilogue, so there is
-// nothing to spread the stores over.
+// Without cross-tile overlap the producer waits for the epilogue, and after a
+// program's last unit no main loop follows: then there is nothing to spread
+// the stores over.
 constexpr int EPI_CHUNKS32 = BN / EPI_COLS;  // 8 fp32 chunks of 32 columns per accumulator row block
 constexpr int EPI_CHUNKS16 = BN / 64;        // 4 chunks of 64 16-bit values
 // Work units shorter than this many K-blocks split each row block's chunks
@@ -510,9 +511,11 @@ constexpr int EPI_CHUNKS16 = BN / 64;        // 4 chunks of 64 16-bit values
 constexpr int EPI_SPLIT_MAX_KB = 12;
 static_assert(EPI_WARPS == 8, "two epilogue warps per TMEM lane quarter");
 
-// Chunk range [c0, c0 + n) of the calling warp (n even, or 0).
-__device__ __forceinline__ void epilogue_chunks(int32_t unit_kblocks, int half, int chunks, int &c0, int &n) {
-    if (unit_kblocks < EPI_SPLIT_MAX_KB) {
+// Chunk range [c0, c0 + n) of the calling warp (n even, or 0). A program's
+// last unit is always split: no MMA runs beside it any more.
+__device__ __forceinline__ void epilogue_chunks(int32_t unit_kblocks, bool last_unit, int half, int chunks,
+                                                int &c0, int &n) {
+    if (unit_kblocks < EPI_SPLIT_MAX_KB || last_unit) {
         n = chunks / 2;
         c0 = half * n;
     } else {
@@ -522,9 +525,9 @@ __device__ __forceinline__ void epilogue_chunks(int32_t unit_kblocks, int half, 
 }
 
 __device__ __forceinline__ uint32_t epilogue_pace_ns(int32_t unit_kblocks, uint32_t cross_tile,
-                                                     int chunks_per_warp) {
+                                                     int chunks_per_warp, bool last_unit) {
     // about 160 ns per K-block of spread over a warp's chunks
-    return (cross_tile && unit_kblocks >= 32 && chunks_per_warp > 0)
+    return (cross_tile && !last_unit && unit_kblocks >= 32 && chunks_per_warp > 0)
                ? uint32_t(unit_kblocks) * 160u / uint32_t(chunks_per_warp)
                : 0u;
 }
@@ -925,15 +928,16 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
                 mbar_arrive(tempty_bar(acc));  // accumulator may be overwritten
             };
             const int64_t col_base = int64_t(tn) * BN;
+            const bool last = tile + grid >= p.num_tiles;
             int c0, n;
             if (p.out_dtype == 0) {
-                epilogue_chunks(num_kb, half, EPI_CHUNKS32, c0, n);
+                epilogue_chunks(num_kb, last, half, EPI_CHUNKS32, c0, n);
                 epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, 0,
-                                         epilogue_pace_ns(num_kb, p.cross_tile, n));
+                                         epilogue_pace_ns(num_kb, p.cross_tile, n, last));
             } else {
-                epilogue_chunks(num_kb, half, EPI_CHUNKS16, c0, n);
+                epilogue_chunks(num_kb, last, half, EPI_CHUNKS16, c0, n);
                 epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
-                                           epilogue_pace_ns(num_kb, p.cross_tile, n));
+                                           epilogue_pace_ns(num_kb, p.cross_tile, n, last));
             }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();

@@ -422,15 +422,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 }
             };
             const int64_t col_base = int64_t(tn) * pair::TILE_N;
+            const bool last = u + num_pairs >= p.num_units;
             int c0, n;
             if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
-                epilogue_chunks(unit_kb, half, EPI_CHUNKS32, c0, n);
+                epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
                 epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split,
-                                         epilogue_pace_ns(unit_kb, p.cross_tile, n));
+                                         epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
             } else {
-                epilogue_chunks(unit_kb, half, EPI_CHUNKS16, c0, n);
+                epilogue_chunks(unit_kb, last, half, EPI_CHUNKS16, c0, n);
                 epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
-                                           epilogue_pace_ns(unit_kb, p.cross_tile, n));
+                                           epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
             }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
