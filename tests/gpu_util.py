@@ -87,6 +87,25 @@ def check_sampled_tiles(C_host, A, B, count=64, seed=0, exact=False, what=""):
             assert_within_bound(got, ref, A, B, f"{what} tile ({r0},{c0})")
 
 
+def check_sampled_rows(C_host, A, B, count=4096, seed=0, exact=False, what=""):
+    """`count` whole rows of C (always the first and the last), every column,
+    against the oracle; `exact` for integer inputs, else the error bound."""
+    M = A.shape[0]
+    if M <= count:
+        rows = np.arange(M)
+    else:
+        rng = np.random.default_rng(seed + 7)
+        inner = rng.choice(np.arange(1, M - 1), size=count - 2, replace=False)
+        rows = np.sort(np.concatenate([[0, M - 1], inner]))
+    ref = oracle.gemm_rows(A, B, rows=rows)
+    got = C_host[rows]
+    if exact:
+        assert np.array_equal(got, ref), f"{what}: sampled rows differ"
+    else:
+        assert_within_bound(got, ref, A, B, f"{what}: {rows.size} sampled rows")
+    return rows.size
+
+
 def check_row_col_sums(C_host, A, B, what=""):
     """Every row sum of C equals A @ (B @ 1) and every column sum equals
     (1^T A) @ B (float64, numpy); a tile written to the wrong place or left

@@ -12,7 +12,8 @@ import torch
 import oracle
 from dense_gemm_gb300 import GemmError, gemm, get_config, sync_status, tile_map, kernel_info
 from dense_gemm_gb300.inputs import WORKLOADS, draw, relayout
-from gpu_util import (assert_within_bound, check_row_col_sums, check_sampled_tiles, require_gpu,
+from gpu_util import (assert_within_bound, check_row_col_sums, check_sampled_rows, check_sampled_tiles,
+                      require_gpu,
                       run, to_dev)
 
 pytestmark = pytest.mark.gpu
@@ -294,6 +295,7 @@ def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=Fal
             B = relayout(B, w.b_layout)
     _, C = run(A, B, grouped=grouped, cross_tile=cross, single_cta=single)
     check_sampled_tiles(C, A, B, count=count, seed=w.seed, exact=exact_dist, what=name)
+    assert check_sampled_rows(C, A, B, count=4096, seed=w.seed, exact=exact_dist, what=name) >= min(4096, w.M)
     check_row_col_sums(C, A, B, what=name)
     return C
 
