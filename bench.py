@@ -48,6 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--group-size", type=int, default=8)
     p.add_argument("--cross-tile", choices=["on", "off"], default="on")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--burst-launches", type=int, default=10,
+                   help="launches of the short burst loop after the timed region (0: skip)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -394,6 +396,19 @@ def run_gpu(args, w):
     med_launch_ms = statistics.median(per_launch_ms)
     achieved = flops / (avg_launch_ms * 1e-3) / 1e12
 
+    # ---- burst: after a 2 s rest, a short loop below the power limit (for the
+    # burst peak; the timed loop above runs at the limit)
+    burst_ms = None
+    if args.burst_launches > 0:
+        time.sleep(2.0)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.burst_launches):
+            step()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        burst_ms = b0.elapsed_time(b1) / args.burst_launches
+
     # ---- end to end: host operands, copies in the timed region
     e2e = None
     if not args.no_e2e and args.e2e_steps > 0:
@@ -436,14 +451,17 @@ def run_gpu(args, w):
         return 0
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    burst_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    # the timed loop is hundreds of back-to-back launches at the power limit:
+    # compare it with the sustained peak (the burst one when there is none)
+    sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
+    peak = sustained or burst_peak
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     compulsory = 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
     intensity = flops / compulsory
     bound_tflops = min(NVL72_SPEC_FP16_TFLOPS, hbm * 1e9 * intensity / 1e12)
     traffic = recorded_traffic(w.name, args.order, cross)
     info = kernel_info(0 if args.single_cta else 4)
-    sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
 
     line = {
         "metric": "FP16 GEMM TFLOPS (2MNK/s) and % of GB300 dense FP16 peak",
@@ -456,13 +474,17 @@ def run_gpu(args, w):
                                             else "CTA pair (cta_group::2), 256x256"}),
         "pct_of_peak": {"nvl72_spec_2500": 100.0 * value / world / NVL72_SPEC_FP16_TFLOPS,
                         "nominal_2250": 100.0 * value / world / NOMINAL_FP16_TFLOPS,
-                        f"{peak_src}_bf16_{peak:g}": 100.0 * value / world / peak},
+                        f"{peak_src}_bf16_burst_{burst_peak:g}": 100.0 * value / world / burst_peak},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} cuBLAS bf16 burst (MEASURED_PEAKS.json) x nominal "
-                                    "fp16/bf16 ratio 1.0",
-                     "frac_of_sustained_peak": (achieved / sustained) if sustained else None,
-                     "sustained_peak": sustained,
+                     "peak_source": (f"{peak_src} cuBLAS bf16 {'sustained' if sustained else 'burst'} "
+                                     "(MEASURED_PEAKS.json) x nominal fp16/bf16 ratio 1.0; the timed "
+                                     "loop runs at the power limit"),
+                     "burst": ({"achieved": flops / (burst_ms * 1e-3) / 1e12, "peak": burst_peak,
+                                "frac": flops / (burst_ms * 1e-3) / 1e12 / burst_peak,
+                                "launches": args.burst_launches, "avg_launch_ms": burst_ms,
+                                "note": "short loop after a 2 s rest, against the burst peak"}
+                               if burst_ms else None),
                      "kernel": ("g16::gemm_f16_persistent<true,true>" if args.single_cta
                                 else "g16::gemm_f16_pair<true,true>"),
                      "algorithmic_flops_per_launch": flops,
