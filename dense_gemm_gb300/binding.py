@@ -17,6 +17,7 @@ SCHED_GROUPED = 0x1
 SCHED_CROSS_TILE = 0x2
 SCHED_SINGLE_CTA = 0x4
 SCHED_NON_PERSISTENT = 0x8
+SCHED_DYNAMIC = 0x10
 
 _STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
            3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT"}
@@ -108,9 +109,10 @@ def gemm_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int,
 
 
 def sched_flags(grouped: bool = True, cross_tile: bool = True, single_cta: bool = False,
-                persistent: bool = True) -> int:
+                persistent: bool = True, dynamic: bool = False) -> int:
     return ((SCHED_GROUPED if grouped else 0) | (SCHED_CROSS_TILE if cross_tile else 0)
-            | (SCHED_SINGLE_CTA if single_cta else 0) | (0 if persistent else SCHED_NON_PERSISTENT))
+            | (SCHED_SINGLE_CTA if single_cta else 0) | (0 if persistent else SCHED_NON_PERSISTENT)
+            | (SCHED_DYNAMIC if dynamic else 0))
 
 
 _OUT_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -118,7 +120,7 @@ _OUT_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
          group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
-         single_cta: bool = False, persistent: bool = True, alpha: float = 1.0,
+         single_cta: bool = False, persistent: bool = True, dynamic: bool = False, alpha: float = 1.0,
          out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
     """C = alpha * (A @ B) with A [M,K], B [K,N] fp16 CUDA tensors.
 
@@ -139,7 +141,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     if out.dtype not in _OUT_CODES or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32/float16/bfloat16 CUDA tensor of shape [M, N]")
-    flags = sched_flags(grouped, cross_tile, single_cta, persistent)
+    flags = sched_flags(grouped, cross_tile, single_cta, persistent, dynamic)
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
@@ -238,9 +240,10 @@ def tile_map(num_m_tiles: int, num_n_tiles: int, group_size_m: int, grouped: boo
     return out
 
 
-def get_config(M: int = 0, N: int = 0, single_cta: bool = False, persistent: bool = True) -> dict:
+def get_config(M: int = 0, N: int = 0, single_cta: bool = False, persistent: bool = True,
+               dynamic: bool = False) -> dict:
     v = [ctypes.c_int32() for _ in range(5)]
-    flags = sched_flags(single_cta=single_cta, persistent=persistent)
+    flags = sched_flags(single_cta=single_cta, persistent=persistent, dynamic=dynamic)
     _check(load_library().gemm_f16_get_config(M, N, flags, *[ctypes.byref(x) for x in v]),
            "gemm_f16_get_config")
     return dict(zip(("bm", "bn", "bk", "stages", "grid"), (x.value for x in v)))

@@ -437,7 +437,11 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     p.wait.timeout_ns = g_timeout_ns.load();
     p.wait.epoch = next_epoch();
 
-    const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT);
+    // dynamic units: one cluster per unit in the grid; the resident clusters take
+    // the others' units through cluster launch control (CTA pairs with TMA loads)
+    const bool dynamic = (schedule_flags & GEMM_SCHED_DYNAMIC) && use_pair && load_tma;
+    p.dynamic = dynamic ? 1u : 0u;
+    const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT) && !dynamic;
     const int programs = !persistent ? p.num_units
                          : use_pair  ? (load_tma ? ds->max_pairs : ds->max_pairs_pred)
                                      : ds->num_sms;
@@ -447,13 +451,13 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     if (log_enabled())
         std::fprintf(stderr,
                      "[gemm_f16] M=%lld N=%lld K=%lld kernel=%s tiles=%d grid=%d load=%s store=%s A=%s "
-                     "B=%s order=%s G=%d cross_tile=%u persistent=%d splits=%d\n",
+                     "B=%s order=%s G=%d cross_tile=%u persistent=%d dynamic=%u splits=%d\n",
                      (long long)M, (long long)N, (long long)K, use_pair ? "cta-pair 256x256" : "one-cta 128x256",
                      p.num_tiles, grid,
                      load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
                      p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
                      grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile, int(persistent),
-                     sp.splits);
+                     p.dynamic, sp.splits);
 
     cudaError_t e;
     if (split) {
@@ -573,7 +577,7 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
             if (cudaGetDevice(&dev) != cudaSuccess || device_init(dev, &ds) != cudaSuccess)
                 return GEMM_ERR_CUDA;
             const int64_t tiles = cdiv(M, tm) * cdiv(N, tn);
-            const int64_t programs = (flags & GEMM_SCHED_NON_PERSISTENT) ? tiles
+            const int64_t programs = (flags & (GEMM_SCHED_NON_PERSISTENT | GEMM_SCHED_DYNAMIC)) ? tiles
                                      : single ? ds->num_sms : ds->max_pairs;
             *grid = int32_t(tiles < programs ? tiles : programs);
         }

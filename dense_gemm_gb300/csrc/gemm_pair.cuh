@@ -40,6 +40,18 @@ constexpr int B_STAGE_BYTES = CTA_N * BK * 2;  // 16 KiB
 constexpr uint32_t PAIR_TX_BYTES = 2u * (A_STAGE_BYTES + B_STAGE_BYTES);
 constexpr int PLACE_WARPS = 4;              // predicated loads: one copy group (64 lines) each per K-block
 static_assert(PLACE_WARPS * GROUP_LINES == CTA_M + CTA_N, "loader shares");
+// Dynamic units (cluster launch control): CTA 0's producer requests the
+// cancellations, both CTAs' producers read the answers and publish the unit
+// sequence into their own CTA's ring of QDEPTH ids. Every reader trails the
+// producer by at most STAGES units (the producer waits for the MMA to free a
+// stage) plus NUM_ACC (the MMA waits for the epilogue to free an accumulator),
+// so slots are reused only after every reader has read them.
+constexpr int QDEPTH = 16;
+static_assert(QDEPTH > STAGES + NUM_ACC + 3, "unit ring shorter than the readers' lag");
+// Cancellation answers arrive in both CTAs (multicast); CTA 1's producer may
+// trail CTA 0's by up to STAGES units, so answers rotate over more slots.
+constexpr int NCLC = 8;
+static_assert(NCLC > STAGES + 1, "answer slots reused before CTA 1 read them");
 
 // Shared-memory map. The predicated-load variant keeps two operand stages and
 // holds the loader warps' staging rings (one mbarrier per slot) instead.
@@ -62,9 +74,14 @@ struct Layout {
     static constexpr int placed_bar0 = 2 * stages + 3 * NUM_ACC + 1;
     static constexpr int copy_bar0 = placed_bar0 + (kTmaLoad ? 0 : stages);
     static constexpr int free_bar0 = copy_bar0 + copy_slots;
-    static constexpr int num_bars = free_bar0 + (kTmaLoad ? 0 : COPY_DEPTH);
+    // cluster launch control: two response slots and their barriers, the unit ring
+    static constexpr int clc_bar0 = free_bar0 + (kTmaLoad ? 0 : COPY_DEPTH);
+    static constexpr int qfull_bar0 = clc_bar0 + NCLC;
+    static constexpr int num_bars = qfull_bar0 + QDEPTH;
     static constexpr int off_tmem_slot = off_bar + num_bars * 8;
-    static constexpr int smem_bytes = off_tmem_slot + 16 + 1024;
+    static constexpr int off_clc_resp = (off_tmem_slot + 16 + 15) / 16 * 16;
+    static constexpr int off_qids = off_clc_resp + NCLC * 16;
+    static constexpr int smem_bytes = off_qids + QDEPTH * 4 + 1024;
     static_assert(off_b % 1024 == 0 && off_epi % 1024 == 0, "swizzled buffers need 1 KiB alignment");
     static_assert(off_copy % 128 == 0, "TMA box destinations need 128-byte alignment");
     static_assert(smem_bytes <= 232448, "exceeds the 227 KiB per-CTA shared memory limit");
@@ -124,6 +141,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             for (int q = 0; q < COPY_DEPTH; ++q) mbar_init(bar0 + 8u * (Lay::free_bar0 + q), pair::PLACE_WARPS);
         }
         for (int q = 0; q < Lay::copy_slots; ++q) mbar_init(bar0 + 8u * (Lay::copy_bar0 + q), 1);
+        for (int q = 0; q < pair::NCLC + pair::QDEPTH; ++q) mbar_init(bar0 + 8u * (Lay::clc_bar0 + q), 1);
         fence_mbar_init();
     }
     if (warp == MMA_WARP) {  // one warp in each CTA of the pair, collectively
@@ -147,6 +165,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int32_t num_kb = p.num_kb;
+
+    // ---- unit sequence of this pair: pair_id, then pair_id + num_pairs, ... (static), or
+    // with dynamic units pair_id (= this cluster's own unit) followed by the units of the
+    // clusters CTA 0's producer cancels, published into the ring.
+    const bool dyn = kTmaLoad && p.dynamic != 0;
+    const uint32_t qids = base + Lay::off_qids;
+    auto qfull_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::qfull_bar0 + q); };
+    // unit number k >= 1 of the sequence is published in ring entry k - 1 (unit 0 is the
+    // cluster's own and never published)
+    auto read_unit = [&](uint32_t k, int32_t &u) -> bool {
+        const uint32_t q = (k - 1) % pair::QDEPTH;
+        if (!mbar_wait_cluster(qfull_bar(q), ((k - 1) / pair::QDEPTH) & 1u, p.wait)) return false;
+        u = ld_shared_s32(qids + 4u * q);
+        return true;
+    };
+    auto next_unit = [&](uint32_t it, int32_t &u) -> bool {  // readers: advance past unit number it
+        if (!dyn) {
+            u += num_pairs;
+            return true;
+        }
+        return read_unit(it + 1, u);
+    };
+    // true if unit number k is known to be the end of the sequence (readers, no waiting)
+    auto known_end = [&](uint32_t k, int32_t u) -> bool {
+        if (!dyn) return u + num_pairs >= p.num_units;
+        const uint32_t q = (k - 1) % pair::QDEPTH;
+        return mbar_test_wait_cluster(qfull_bar(q), ((k - 1) / pair::QDEPTH) & 1u) &&
+               ld_shared_s32(qids + 4u * q) < 0;
+    };
 
     if (!kTmaLoad && warp < LOAD_WARPS) {
         // ============================================================ predicated loads (both CTAs)
@@ -249,7 +296,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             int32_t it = 0;
-            for (int32_t u = pair_id; ok && u < p.num_units; u += num_pairs, ++it) {
+            // dynamic units: CTA 0 asks for the next cluster's cancellation one unit
+            // ahead; the answer lands in both CTAs, whose producers each arm their own
+            // barrier for it, read it and publish the unit into their CTA's ring
+            uint32_t requested = 0, answered = 0;
+            bool ended = false;
+            auto clc_resp = [&](uint32_t i) { return base + Lay::off_clc_resp + 16u * (i % pair::NCLC); };
+            auto clc_bar = [&](uint32_t i) { return bar0 + 8u * (Lay::clc_bar0 + i % pair::NCLC); };
+            auto request = [&] {  // CTA 0
+                mbar_arrive_expect_tx(clc_bar(requested), 16);
+                clc_try_cancel_all(clc_resp(requested), clc_bar(requested));
+                ++requested;
+            };
+            auto publish = [&](uint32_t k, int32_t id) {  // unit number k >= 1 -> ring entry k - 1
+                const uint32_t q = (k - 1) % pair::QDEPTH;
+                st_shared_s32(qids + 4u * q, id);
+                mbar_arrive(qfull_bar(q));
+            };
+            if (dyn && rank == 0) request();
+            for (int32_t u = pair_id; ok && u >= 0 && u < p.num_units; ++it) {
                 const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
                 const int32_t kb0 = split * p.kb_per_split;
                 const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
@@ -304,7 +369,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                     ++issued;
                     if (++stage == NST) { stage = 0; phase ^= 1u; }
                 }
+                if (!ok) break;
+                // ---- the next unit
+                if (!dyn) {
+                    u += num_pairs;
+                } else {
+                    int32_t nx = -1;
+                    if (!ended) {
+                        if (rank != 0) mbar_arrive_expect_tx(clc_bar(answered), 16);  // this CTA's copy
+                        if (!mbar_wait(clc_bar(answered), (answered / pair::NCLC) & 1u, p.wait)) {
+                            ok = false;
+                            break;
+                        }
+                        const int32_t x = clc_cancelled_ctaid_x(clc_resp(answered));
+                        ++answered;
+                        nx = x < 0 ? -1 : (x >> 1);  // a failed request ends the sequence: ask no more
+                        ended = nx < 0;
+                        if (rank == 0 && nx >= 0) request();
+                    }
+                    publish(uint32_t(it) + 1, nx);
+                    u = nx;
+                }
             }
+            // no cancellation answer may still be on its way into shared memory
+            for (uint32_t i = answered; i < requested; ++i)
+                mbar_wait_slow(clc_bar(i), (i / pair::NCLC) & 1u, cleanup_wait(p.wait), false);
             if (!ok) {
                 if (rank == 0) {
                     // Let the copies counted on this CTA's barriers land before exiting.
@@ -357,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             const DescStep da = make_desc_step(sA, p.a_mn, pair::A_STAGE_BYTES);
             const DescStep db = make_desc_step(sB, p.b_mn, pair::B_STAGE_BYTES);
             const uint32_t idesc = p.idesc;
-            for (int32_t u = pair_id; ok && u < p.num_units; u += num_pairs, ++it) {
+            for (int32_t u = pair_id; ok && u >= 0 && u < p.num_units; ++it) {
                 const int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
                 const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
                 const uint32_t acc = it & 1, use = it >> 1;
@@ -390,6 +479,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 }
                 if (!ok) break;
                 mma_commit_pair_mc_elect(tfull_bar(acc), 0x3);  // both halves of the tile complete
+                if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) {
+                    ok = false;
+                    break;
+                }
             }
             mma_commit_pair_elect(drain_bar);
             __all_sync(0xffffffffu, mbar_wait_slow(drain_bar, 0, cleanup_wait(p.wait), false));
@@ -401,7 +494,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         const int half = ew / 4;
         const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         int32_t it = 0;
-        for (int32_t u = pair_id; u < p.num_units; u += num_pairs, ++it) {
+        for (int32_t u = pair_id; u >= 0 && u < p.num_units; ++it) {
             const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
             const int32_t kb0 = split * p.kb_per_split;
             const int32_t unit_kb = min(num_kb, kb0 + p.kb_per_split) - kb0;
@@ -422,7 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 }
             };
             const int64_t col_base = int64_t(tn) * pair::TILE_N;
-            const bool last = u + num_pairs >= p.num_units;
+            // no unit follows (dynamic units: if already published)
+            const bool last = __shfl_sync(0xffffffffu, known_end(uint32_t(it) + 1, u) ? 1 : 0, 0) != 0;
             int c0, n;
             if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
@@ -433,6 +527,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
                                            epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
             }
+            if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) break;
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

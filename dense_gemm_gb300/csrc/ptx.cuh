@@ -47,6 +47,86 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test: true once the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// As mbar_test_wait, acquiring at cluster scope (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ void st_shared_s32(uint32_t addr, int32_t v) {
+    asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_shared_s32(uint32_t addr) {
+    int32_t v;
+    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// st.shared::cluster: a 32-bit store into the shared memory of the CTA that
+// `cluster_addr` (from mapa) points into.
+__device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int32_t v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Requests the cancellation of a cluster of this grid that has not started
+// running; the 16-byte response lands at `resp` (16-byte aligned) and
+// completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            resp),
+        "r"(bar)
+        : "memory");
+}
+
+// As clc_try_cancel, with the response written to the same offset in every CTA
+// of the cluster, each completing 16 bytes on its own barrier at `bar`'s offset.
+__device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128"
+        " [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// The first CTA x-index of the cluster a response cancelled, or -1 if the
+// request failed (no cluster left to cancel).
+__device__ __forceinline__ int32_t clc_cancelled_ctaid_x(uint32_t resp) {
+    uint32_t valid, x = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %1, 1, 0, p;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, _, _, _}, r;\n\t}"
+        : "+r"(x), "=r"(valid)
+        : "r"(resp)
+        : "memory");
+    return valid ? int32_t(x) : -1;
+}
+
 // ---------------------------------------------------------------- proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

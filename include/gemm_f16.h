@@ -63,7 +63,11 @@ typedef enum {
 #define GEMM_SCHED_NON_PERSISTENT 0x8u /* one program per tile (grid = #tiles, the hardware
                                           assigns programs to SMs) instead of a persistent
                                           grid of co-resident programs */
-#define GEMM_SCHED_ALL_FLAGS 0xFu
+#define GEMM_SCHED_DYNAMIC 0x10u /* CTA-pair tiles with TMA-loadable A and B: launch one
+                                     cluster per tile and let resident clusters take the
+                                     tiles of clusters that have not started (cluster launch
+                                     control), in ascending tile_id; ignored otherwise */
+#define GEMM_SCHED_ALL_FLAGS 0x1Fu
 
 /*
  * gemm_f16 — C = A @ B.
@@ -96,7 +100,10 @@ typedef enum {
  * the persistent order is a CTA pair or a CTA.
  * GEMM_SCHED_NON_PERSISTENT launches one program per tile ([persistent]
  * "naive tiled matmul" grid); program p then computes tile_id p only, and
- * GEMM_SCHED_CROSS_TILE has nothing to overlap.
+ * GEMM_SCHED_CROSS_TILE has nothing to overlap. GEMM_SCHED_DYNAMIC (no
+ * counterpart on the pages) keeps programs resident like the persistent order
+ * but hands out tiles as programs become free instead of tile_id = pid + i*grid;
+ * the tile map itself is unchanged.
  * Sizes: M, N, K >= 0, each < 2^31. M == 0 or N == 0: nothing is done.
  * K == 0: C is set to 0.
  * Returns GEMM_OK once the work is enqueued.

@@ -55,7 +55,7 @@ def _call(lib, **kw):
 
 @pytest.mark.parametrize("kw", [dict(M=-1), dict(N=-5), dict(K=-1), dict(M=2 ** 31),
                                 dict(sam=0), dict(sak=-1), dict(sbk=0), dict(sbn=0), dict(scm=0),
-                                dict(scn=0), dict(G=0), dict(G=-3), dict(flags=16),
+                                dict(scn=0), dict(G=0), dict(G=-3), dict(flags=32),
                                 dict(flags=0x80000000), dict(C=0), dict(A=0), dict(B=0),
                                 dict(scm=3)])
 def test_invalid_arguments(lib, kw):
@@ -95,7 +95,7 @@ def test_config_without_device(lib):
     cfg = get_config(0, 0, single_cta=True)
     assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (128, 256, 64)
     assert lib.gemm_f16_get_config(-1, 4, 0, None, None, None, None, None) == 1
-    assert lib.gemm_f16_get_config(4, 4, 16, None, None, None, None, None) == 1
+    assert lib.gemm_f16_get_config(4, 4, 32, None, None, None, None, None) == 1
 
 
 def test_wait_timeout_validation(lib):

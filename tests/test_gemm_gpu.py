@@ -283,9 +283,46 @@ def test_calls_captured_in_a_cuda_graph():
                                   oracle.round_output(ref, "f16"))
 
 
+@pytest.mark.parametrize("shape", [(256, 256, 64), (512, 512, 512), (1000, 1200, 320),
+                                   (2304, 2560, 640), (4096, 4096, 256),
+                                   (16384, 16384, 64)])  # ~54 tiles per CTA pair: the unit ring wraps
+@pytest.mark.parametrize("grouped,cross", [(True, True), (False, True), (True, False)])
+def test_dynamic_units_bit_exact(shape, grouped, cross):
+    """GEMM_SCHED_DYNAMIC: every tile computed exactly once whichever cluster
+    takes it (fewer tiles than CTA pairs, ragged edges, many tiles per pair)."""
+    M, N, K = shape
+    A = draw(M, K, "int", 95)
+    B = draw(K, N, "int", 96)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross, G=3, dynamic=True)
+    assert np.array_equal(C, oracle.gemm(A, B))
+    assert sync_status() == 0
+    cfg = get_config(M, N, dynamic=True)
+    assert cfg["grid"] == -(-M // cfg["bm"]) * -(-N // cfg["bn"])
+
+
+def test_dynamic_units_match_static_bitwise():
+    """A tile's arithmetic does not depend on which cluster computes it, so the
+    dynamic and the static orders give identical bits on random operands."""
+    A = draw(2304, 640, "normal", 99)
+    B = draw(640, 2560, "normal", 100)
+    _, Cs = run(A, B, G=8)
+    _, Cd = run(A, B, G=8, dynamic=True)
+    assert np.array_equal(Cs, Cd)
+    assert_within_bound(Cd, oracle.gemm(A, B), A, B, "dynamic 2304x2560x640")
+
+
+def test_dynamic_units_ignored_on_predicated_and_single_cta_paths():
+    A = draw(300, 257, "int", 97)
+    B = draw(257, 520, "int", 98)
+    ref = oracle.gemm(A, B)
+    for single in (False, True):
+        _, C = run(A, B, single_cta=single, dynamic=True)
+        assert np.array_equal(C, ref)
+
+
 # ------------------------------------------------------------------ full workload sizes
 
-def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=False):
+def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=False, dynamic=False):
     w = WORKLOADS[name]
     A, B = w.operands()
     if exact_dist:
@@ -293,7 +330,7 @@ def _full(name, grouped=True, cross=True, exact_dist=False, count=64, single=Fal
         B = draw(w.K, w.N, "int", w.seed + 1)
         if w.b_layout != "row":
             B = relayout(B, w.b_layout)
-    _, C = run(A, B, grouped=grouped, cross_tile=cross, single_cta=single)
+    _, C = run(A, B, grouped=grouped, cross_tile=cross, single_cta=single, dynamic=dynamic)
     check_sampled_tiles(C, A, B, count=count, seed=w.seed, exact=exact_dist, what=name)
     assert check_sampled_rows(C, A, B, count=4096, seed=w.seed, exact=exact_dist, what=name) >= min(4096, w.M)
     check_row_col_sums(C, A, B, what=name)
@@ -311,6 +348,10 @@ def test_full_square_512(grouped):
 @pytest.mark.parametrize("grouped", [True, False])
 def test_full_8192x8192x4096(grouped):
     _full("square_8192x8192x4096", grouped=grouped)
+
+
+def test_full_8192x8192x4096_dynamic():
+    _full("square_8192x8192x4096", grouped=True, dynamic=True, count=16)
 
 
 def test_full_16384x16384x4096_headline():
