@@ -327,7 +327,13 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     const bool a_tma = a_k ? tma_ok(A, K, stride_am, 2) : tma_ok(A, M, stride_ak, 2);
     const bool b_tma = b_n ? tma_ok(B, N, stride_bk, 2) : tma_ok(B, K, stride_bn, 2);
     const bool load_tma = a_tma && b_tma;
-    const bool store_tma = tma_ok(C, N, stride_cm, esize);
+    // A TMA store clipped inside a 16-byte granule writes the whole granule
+    // (measured: an fp32 C with N = 513 inside rows of 520 had columns 513..515
+    // overwritten). C's map therefore ends at the last granule boundary before
+    // column N and the kernel stores the rest of each row itself; with no whole
+    // granule in a row, C takes the plain-store path.
+    const int64_t n_granule = N & ~int64_t(16 / esize - 1);
+    const bool store_tma = tma_ok(C, N, stride_cm, esize) && n_granule > 0;
     // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
     const bool use_pair = !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
     if (sk.enabled && !(use_pair && load_tma)) return GEMM_ERR_UNSUPPORTED;  // split-K: CTA pairs, TMA loads
@@ -386,7 +392,8 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                        : out_dtype == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         // one 128-byte row of the box: 32 fp32 or 64 16-bit elements, 32 rows
-        if (!encode_2d(&tmC, dt, C, N, M, stride_cm * esize, 128 / esize, 32)) return GEMM_ERR_CUDA;
+        if (!encode_2d(&tmC, dt, C, uint64_t(n_granule), M, stride_cm * esize, 128 / esize, 32))
+            return GEMM_ERR_CUDA;
     }
 
     Params p;

@@ -77,6 +77,8 @@ typedef enum {
  *
  * A: __half[M,K] (device), B: __half[K,N] (device), C: float[M,N] (device).
  * C is overwritten and never read; it must not overlap A or B (undefined).
+ * Only the M x N elements are written: memory between rows (stride_cm > N)
+ * keeps its contents.
  * group_size_m: GROUP_SIZE_M of the grouped order, >= 1 when
  *   GEMM_SCHED_GROUPED is set (ignored otherwise; G >= #m-tiles gives one
  *   group, G == 1 gives the row-major order).

@@ -155,6 +155,48 @@ def test_predicated_paths_bit_exact(case):
             assert np.isnan(buf[mask]).all(), name
 
 
+OUT_TYPES = [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")]
+
+
+@pytest.mark.parametrize("dtype,name", OUT_TYPES)
+@pytest.mark.parametrize("N", [513, 509, 4, 3, 1])
+@pytest.mark.parametrize("single", [False, True])
+def test_c_views_keep_their_padding_columns(dtype, name, N, single):
+    """C a view of a wider buffer (aligned rows, N not a multiple of the 16-byte
+    granule): a TMA store clipped inside a granule writes the whole granule, so
+    the kernel must end C's map on the last granule boundary and store the rest
+    itself. Every column past N keeps its NaN."""
+    M, K, ld = 260, 64, 520
+    A = draw(M, K, "int", 450 + N)
+    B = draw(K, N, "int", 451 + N)
+    want = oracle.round_output(oracle.gemm(A, B), name, 1.0)
+    buf = torch.full((M * ld,), float("nan"), dtype=dtype, device="cuda")
+    C = buf.as_strided((M, N), (ld, 1), 0)
+    gemm(to_dev(A), to_dev(B), C, single_cta=single)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.double().cpu().numpy(), want)
+    pad = buf.view(M, ld)[:, N:].float().cpu().numpy()
+    assert np.isnan(pad).all(), f"{int((~np.isnan(pad)).sum())} padding values written"
+
+
+def test_operand_padding_at_the_k_edge_is_not_read():
+    """K = 250 inside rows of 256 (TMA loads): the padding holds NaN, and TMA
+    zero-fills per element, so the product is exact."""
+    M, N, K = 300, 400, 250
+    A0 = draw(M, K, "int", 460)
+    B0 = draw(K, N, "int", 461)
+    ref = oracle.gemm(A0, B0)
+    Ab = torch.full((M, 256), float("nan"), dtype=torch.float16)
+    Ab[:, :K] = A0
+    Bc = torch.full((N, 256), float("nan"), dtype=torch.float16)
+    Bc[:, :K] = B0.t()
+    for single in (False, True):
+        _, C = run(Ab[:, :K], B0, single_cta=single)
+        assert np.array_equal(C, ref)
+        _, C = run(A0, Bc[:, :K].t(), single_cta=single)
+        assert np.array_equal(C, ref)
+
+
 def test_predicated_random_within_bound():
     A = relayout(draw(600, 257, "uniform", 51), "row")
     B = relayout(draw(257, 700, "uniform", 52), "col")
@@ -478,7 +520,6 @@ def test_splitk_rejects_small_workspace_and_unaligned_operands():
 
 # ------------------------------------------------------------------ 16-bit C and alpha
 
-OUT_TYPES = [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")]
 
 
 @pytest.mark.parametrize("dtype,name", OUT_TYPES)
