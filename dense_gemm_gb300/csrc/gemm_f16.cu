@@ -55,9 +55,9 @@ cudaError_t set_smem_attr() {
                                 Layout<L>::smem_bytes);
 }
 
-template <bool L, bool S>
+template <bool L, bool S, bool D = false>
 cudaError_t set_pair_smem_attr() {
-    return cudaFuncSetAttribute(gemm_f16_pair<L, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_f16_pair<L, S, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 pair::Layout<L>::smem_bytes);
 }
 
@@ -97,6 +97,8 @@ cudaError_t device_init(int dev, DeviceState **out) {
         if (e == cudaSuccess) e = set_pair_smem_attr<true, false>();
         if (e == cudaSuccess) e = set_pair_smem_attr<false, true>();
         if (e == cudaSuccess) e = set_pair_smem_attr<false, false>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<true, true, true>();
+        if (e == cudaSuccess) e = set_pair_smem_attr<true, false, true>();
         if (e == cudaSuccess) d.max_pairs = query_max_pairs<true>(d.num_sms);
         if (e == cudaSuccess) d.max_pairs_pred = query_max_pairs<false>(d.num_sms);
         d.init_err = e;
@@ -202,12 +204,12 @@ cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap
     return cudaGetLastError();
 }
 
-template <bool L, bool S>
+template <bool L, bool S, bool D = false>
 cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
                         const ClassMaps &cm, int grid, cudaStream_t stream) {
     constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
     if constexpr (L)
-        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, p, NoClassMaps{});
+        gemm_f16_pair<L, S, D><<<grid, threads, smem, stream>>>(a, b, c, p, NoClassMaps{});
     else
         gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, p, cm);
     return cudaGetLastError();
@@ -329,11 +331,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     const bool load_tma = a_tma && b_tma;
     // A TMA store clipped inside a 16-byte granule writes the whole granule
     // (measured: an fp32 C with N = 513 inside rows of 520 had columns 513..515
-    // overwritten). C's map therefore ends at the last granule boundary before
-    // column N and the kernel stores the rest of each row itself; with no whole
-    // granule in a row, C takes the plain-store path.
-    const int64_t n_granule = N & ~int64_t(16 / esize - 1);
-    const bool store_tma = tma_ok(C, N, stride_cm, esize) && n_granule > 0;
+    // overwritten), so C goes through TMA only when its rows end on a granule;
+    // a view with N mod 4 (fp32) or N mod 8 (16-bit) != 0 takes plain stores.
+    const bool store_tma = tma_ok(C, N, stride_cm, esize) && (N * esize) % 16 == 0;
     // CTA pairs need TMA loads (both CTAs' copies count on one barrier)
     const bool use_pair = !(schedule_flags & GEMM_SCHED_SINGLE_CTA);
     if (sk.enabled && !(use_pair && load_tma)) return GEMM_ERR_UNSUPPORTED;  // split-K: CTA pairs, TMA loads
@@ -392,8 +392,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                        : out_dtype == GEMM_OUT_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         // one 128-byte row of the box: 32 fp32 or 64 16-bit elements, 32 rows
-        if (!encode_2d(&tmC, dt, C, uint64_t(n_granule), M, stride_cm * esize, 128 / esize, 32))
-            return GEMM_ERR_CUDA;
+        if (!encode_2d(&tmC, dt, C, N, M, stride_cm * esize, 128 / esize, 32)) return GEMM_ERR_CUDA;
     }
 
     Params p;
@@ -468,7 +467,8 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
 
     cudaError_t e;
     if (split) {
-        e = launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
+        e = dynamic ? launch_pair<true, true, true>(tmA, tmB, tmC, p, cm, grid, stream)
+                    : launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
         if (e == cudaSuccess) {
             const int64_t quads = M * ((N + 3) / 4);
             const int threads = 256;
@@ -478,6 +478,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                                               sp.ldw, stride_cm, sp.splits, out_dtype, alpha);
             e = cudaGetLastError();
         }
+    } else if (dynamic) {
+        e = store_tma ? launch_pair<true, true, true>(tmA, tmB, tmC, p, cm, grid, stream)
+                      : launch_pair<true, false, true>(tmA, tmB, tmC, p, cm, grid, stream);
     } else if (use_pair) {
         if (load_tma)
             e = store_tma ? launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream)
@@ -594,7 +597,7 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
 
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
                                    int32_t *dynamic_smem, int32_t *threads) {
-    if (variant < 0 || variant > 7) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 9) return GEMM_ERR_INVALID_ARG;
     cudaFuncAttributes a;
     cudaError_t e;
     int thr, dyn;
@@ -606,7 +609,9 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *stat
         case 4: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
         case 5: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
         case 6: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, true>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
-        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
+        case 7: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
+        case 8: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
     }
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;

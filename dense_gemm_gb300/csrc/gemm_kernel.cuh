@@ -549,13 +549,8 @@ __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, i
             st_shared_v4(stg + swz128(lane, u), v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        // C's map ends at its last 16-byte granule boundary, ne: a TMA store
-        // clipped inside a granule writes the whole granule, which would reach
-        // past column N - 1 into the caller's memory. The split-K workspace has
-        // padded rows of its own, and its map ends at N.
-        const int64_t ne = p.splits > 1 ? p.N : (p.N & ~int64_t(3));
         if (lane == 0) {
-            if (row0 < p.M && col0 < ne) {
+            if (row0 < p.M && col0 < p.N) {
                 if (p.splits > 1)  // partial tile -> workspace slice `split`, read once by the reduction
                     tma_store_3d_hint(tmC, stg, int32_t(col0), int32_t(row0), split, l2_policy_evict_normal());
                 else if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
@@ -564,18 +559,6 @@ __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, i
                     tma_store_2d(tmC, stg, int32_t(col0), int32_t(row0));
             }
             bulk_commit_group();
-        }
-        if (p.splits == 1 && col0 + 32 > ne && col0 < p.N && row0 + lane < p.M) {  // columns ne .. N - 1
-            const int k0 = int(ne - col0);  // a multiple of 4 in [0, 32)
-            float *dst = p.C + (row0 + lane) * p.scm + ne;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (4 * u == k0) {
-#pragma unroll
-                    for (int j = 0; j < 3; ++j)
-                        if (ne + j < p.N) dst[j] = __uint_as_float(v[4 * u + j]);
-                }
-            }
         }
     } else {
         __syncwarp();  // every lane has read the buffer's previous contents
@@ -654,23 +637,10 @@ __device__ __forceinline__ void store_chunk16(uint32_t (&w)[32], int64_t row0, i
             st_shared_v4(stg + swz128(lane, u), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         fence_proxy_async_smem();
         __syncwarp();
-        const int64_t ne = p.N & ~int64_t(7);  // the map ends on a 16-byte granule (see store_chunk32)
         if (lane == 0) {
-            if (row0 < p.M && col0 < ne)
+            if (row0 < p.M && col0 < p.N)
                 tma_store_2d_hint(tmC, stg, int32_t(col0), int32_t(row0), l2_policy_evict_first());
             bulk_commit_group();
-        }
-        if (col0 + 64 > ne && col0 < p.N && row0 + lane < p.M) {  // columns ne .. N - 1
-            const int k0 = int(ne - col0);                        // a multiple of 8 in [0, 64)
-            uint16_t *dst = reinterpret_cast<uint16_t *>(p.C) + (row0 + lane) * p.scm + ne;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (8 * u == k0) {
-#pragma unroll
-                    for (int j = 0; j < 7; ++j)
-                        if (ne + j < p.N) dst[j] = uint16_t(w[4 * u + j / 2] >> (16 * (j & 1)));
-                }
-            }
         }
     } else {
         __syncwarp();

@@ -90,7 +90,9 @@ constexpr int SMEM_BYTES = Layout<true>::smem_bytes;
 constexpr int THREADS = Layout<true>::threads;
 }  // namespace pair
 
-template <bool kTmaLoad, bool kTmaStore>
+// kDyn: units handed out by cluster launch control (TMA loads only); a
+// separate instantiation, so the static schedule carries none of its code.
+template <bool kTmaLoad, bool kTmaStore, bool kDyn = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoad>::threads, 1)
     gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmC, const Params p,
@@ -169,7 +171,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     // ---- unit sequence of this pair: pair_id, then pair_id + num_pairs, ... (static), or
     // with dynamic units pair_id (= this cluster's own unit) followed by the units of the
     // clusters CTA 0's producer cancels, published into the ring.
-    const bool dyn = kTmaLoad && p.dynamic != 0;
+    static_assert(!kDyn || kTmaLoad, "dynamic units need TMA loads");
+    constexpr bool dyn = kDyn;
     const uint32_t qids = base + Lay::off_qids;
     auto qfull_bar = [&](uint32_t q) { return bar0 + 8u * (Lay::qfull_bar0 + q); };
     // unit number k >= 1 of the sequence is published in ring entry k - 1 (unit 0 is the
@@ -314,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 mbar_arrive(qfull_bar(q));
             };
             if (dyn && rank == 0) request();
-            for (int32_t u = pair_id; ok && u >= 0 && u < p.num_units; ++it) {
+            for (int32_t u = pair_id; ok && (!kDyn || u >= 0) && u < p.num_units; ++it) {
                 const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
                 const int32_t kb0 = split * p.kb_per_split;
                 const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
@@ -446,7 +449,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             const DescStep da = make_desc_step(sA, p.a_mn, pair::A_STAGE_BYTES);
             const DescStep db = make_desc_step(sB, p.b_mn, pair::B_STAGE_BYTES);
             const uint32_t idesc = p.idesc;
-            for (int32_t u = pair_id; ok && u >= 0 && u < p.num_units; ++it) {
+            for (int32_t u = pair_id; ok && (!kDyn || u >= 0) && u < p.num_units; ++it) {
                 const int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
                 const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
                 const uint32_t acc = it & 1, use = it >> 1;
@@ -479,9 +482,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 }
                 if (!ok) break;
                 mma_commit_pair_mc_elect(tfull_bar(acc), 0x3);  // both halves of the tile complete
-                if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) {
-                    ok = false;
-                    break;
+                if constexpr (kDyn) {
+                    if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) {
+                        ok = false;
+                        break;
+                    }
+                } else {
+                    u += num_pairs;
                 }
             }
             mma_commit_pair_elect(drain_bar);
@@ -494,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         const int half = ew / 4;
         const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         int32_t it = 0;
-        for (int32_t u = pair_id; u >= 0 && u < p.num_units; ++it) {
+        for (int32_t u = pair_id; (!kDyn || u >= 0) && u < p.num_units; ++it) {
             const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
             const int32_t kb0 = split * p.kb_per_split;
             const int32_t unit_kb = min(num_kb, kb0 + p.kb_per_split) - kb0;
@@ -516,7 +523,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             };
             const int64_t col_base = int64_t(tn) * pair::TILE_N;
             // no unit follows (dynamic units: if already published)
-            const bool last = __shfl_sync(0xffffffffu, known_end(uint32_t(it) + 1, u) ? 1 : 0, 0) != 0;
+            bool last;
+            if constexpr (kDyn)
+                last = __shfl_sync(0xffffffffu, known_end(uint32_t(it) + 1, u) ? 1 : 0, 0) != 0;
+            else
+                last = u + num_pairs >= p.num_units;
             int c0, n;
             if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
@@ -527,7 +538,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
                                            epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
             }
-            if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) break;
+            if constexpr (kDyn) {
+                if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) break;
+            } else {
+                u += num_pairs;
+            }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
         __syncwarp();

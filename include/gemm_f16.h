@@ -246,7 +246,8 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags,
  * (cudaFuncGetAttributes). One-CTA tiles: variant 0 = TMA loads + TMA store,
  * 1 = TMA loads + predicated store, 2 = predicated loads + TMA store,
  * 3 = predicated loads + predicated store. CTA-pair tiles, in the same
- * order: 4, 5, 6, 7. Outputs may be NULL. Needs a device.
+ * order: 4, 5, 6, 7; with GEMM_SCHED_DYNAMIC (TMA loads): 8 = TMA store,
+ * 9 = predicated store. Outputs may be NULL. Needs a device.
  */
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *static_smem, int32_t *dynamic_smem,

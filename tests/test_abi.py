@@ -107,7 +107,7 @@ def test_wait_timeout_validation(lib):
 
 def test_kernel_info_rejects_unknown_variant(lib):
     i32 = ctypes.POINTER(ctypes.c_int32)
-    assert lib.gemm_f16_kernel_info(8, i32(), i32(), i32(), i32()) == 1
+    assert lib.gemm_f16_kernel_info(10, i32(), i32(), i32(), i32()) == 1
     assert lib.gemm_f16_kernel_info(-1, i32(), i32(), i32(), i32()) == 1
 
 

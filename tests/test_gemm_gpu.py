@@ -264,8 +264,8 @@ def test_invalid_arguments_raise():
 
 def test_kernel_resources():
     # warps: producer (1; predicated loads: 3 for one CTA, 4 + 1 issuer per CTA of a pair) + MMA + 8 epilogue
-    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448}
-    for v in range(8):
+    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448, 8: 320, 9: 320}
+    for v in range(10):
         info = kernel_info(v)
         assert info["dynamic_smem"] <= 232448 and info["regs_per_thread"] <= 255
         assert info["threads_per_cta"] == threads[v]
