@@ -486,7 +486,7 @@ def run_gpu(args, w):
                                 "note": "short loop after a 2 s rest, against the burst peak"}
                                if burst_ms else None),
                      "kernel": ("g16::gemm_f16_persistent<true,true>" if args.single_cta
-                                else "g16::gemm_f16_pair<true,true>"),
+                                else "g16::gemm_f16_pair<true,true,false>"),
                      "algorithmic_flops_per_launch": flops,
                      "avg_launch_ms": avg_launch_ms, "median_launch_ms": med_launch_ms,
                      "workload_roofline_tflops_min_P_BWxI": bound_tflops,
