@@ -58,7 +58,7 @@ def parse_args(argv=None):
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
     p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
-                                       "outdtype", "ragged"],
+                                       "outdtype", "ragged", "schedule"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
@@ -522,7 +522,9 @@ def run_sweep(args):
     outdtype - fp32 vs fp16 vs bf16 C (gemm_f16_out) on the headline workload
                and at K = 512, where the C store dominates the traffic;
     ragged - the two ragged workloads (4000 x 5000 x 3000 through TMA, 8191^2 x 257
-             with 514-byte rows through the predicated-load path) and 512^3."""
+             with 514-byte rows through the predicated-load path) and 512^3;
+    schedule - the static pid + i*P tile stream vs GEMM_SCHED_DYNAMIC (cluster
+               launch control) on 8192^2 x 4096, 16384^2 x 1024, 4000 x 5000 x 3000."""
     import torch
     from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
@@ -537,6 +539,9 @@ def run_sweep(args):
     elif args.sweep == "ragged":
         names = ["ragged_4000x5000x3000", "ragged_8191x8191x257", "square_512"]
         points = [dict(grouped=True, cross_tile=True, single_cta=False)]
+    elif args.sweep == "schedule":
+        names = ["square_8192x8192x4096", "ksweep_16384x16384x1024", "ragged_4000x5000x3000"]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False, dynamic=d) for d in (False, True)]
     elif args.sweep == "outdtype":
         names = [HEADLINE, "ksweep_16384x16384x512"]
         points = [("out", torch.float32), ("out", torch.float16), ("out", torch.bfloat16)]
