@@ -83,26 +83,11 @@ __device__ __forceinline__ int32_t ld_shared_s32(uint32_t addr) {
     return v;
 }
 
-// st.shared::cluster: a 32-bit store into the shared memory of the CTA that
-// `cluster_addr` (from mapa) points into.
-__device__ __forceinline__ void st_cluster_s32(uint32_t cluster_addr, int32_t v) {
-    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-
 // ---------------------------------------------------------------- cluster launch control
 // Requests the cancellation of a cluster of this grid that has not started
-// running; the 16-byte response lands at `resp` (16-byte aligned) and
-// completes 16 transaction bytes on `bar`.
-__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
-    asm volatile(
-        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-            resp),
-        "r"(bar)
-        : "memory");
-}
-
-// As clc_try_cancel, with the response written to the same offset in every CTA
-// of the cluster, each completing 16 bytes on its own barrier at `bar`'s offset.
+// running. The 16-byte response is written to offset `resp` (16-byte aligned) in
+// every CTA of the cluster, each completing 16 transaction bytes on its own
+// barrier at `bar`'s offset.
 __device__ __forceinline__ void clc_try_cancel_all(uint32_t resp, uint32_t bar) {
     asm volatile(
         "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128"
@@ -191,23 +176,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]; fp16 x fp16 -> fp32, one CTA.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive (once) on `bar` when every tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -247,18 +215,6 @@ __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_
                  : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                  : "r"(addr)
                  : "memory");
-}
-
-__device__ __forceinline__ void ld_shared_v2(uint32_t addr, uint32_t &a, uint32_t &b) {
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
-    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
 }  // namespace g16
@@ -328,32 +284,6 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
-// D (both CTAs' TMEM) (+)= A (both CTAs' smem, split along M) * B (split along N).
-__device__ __forceinline__ void mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at local offset `bar` in every CTA of `cta_mask`
-// when all tcgen05 ops issued so far by this thread are done.
-__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
 }  // namespace g16
 
 // ---------------------------------------------------------------- L2 cache policies
@@ -375,15 +305,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void *tmap, int32_t x, int32_t y,
-                                                 uint32_t bar, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
-        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, int32_t x,
@@ -412,6 +333,8 @@ __device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src
 // warp-uniform code lets the descriptors live in uniform registers.
 namespace g16 {
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]: fp16 x fp16 -> fp32 on one CTA;
+// accumulate == 0 overwrites D.
 __device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -423,6 +346,8 @@ __device__ __forceinline__ void mma_f16_elect(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// The same on a CTA pair: D in both CTAs' TMEM, A split along M and B along N
+// between the two CTAs' shared memory.
 __device__ __forceinline__ void mma_f16_pair_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                    uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -434,6 +359,7 @@ __device__ __forceinline__ void mma_f16_pair_elect(uint32_t d_tmem, uint64_t a_d
         : "memory");
 }
 
+// Arrives once on `bar` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred pe;\n\t"
@@ -442,6 +368,8 @@ __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
         : "memory");
 }
 
+// Pair form: arrives once on the barrier at `bar`'s offset in every CTA of
+// `cta_mask` when every tcgen05 op this thread issued so far is done.
 __device__ __forceinline__ void mma_commit_pair_mc_elect(uint32_t bar, uint16_t cta_mask) {
     asm volatile(
         "{\n\t.reg .pred pe;\n\t"
@@ -452,6 +380,7 @@ __device__ __forceinline__ void mma_commit_pair_mc_elect(uint32_t bar, uint16_t 
         : "memory");
 }
 
+// Pair form with a single barrier (`bar` a shared::cluster address).
 __device__ __forceinline__ void mma_commit_pair_elect(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred pe;\n\t"
