@@ -222,7 +222,10 @@ gemm_status_t gemm_f16_splitk_noalloc(const void *A, const void *B, float *C,
  * tile_id receives {program id that processes it, tile_m, tile_n} where
  * program p visits tile_id = p, p + grid, p + 2*grid, ...
  * grid >= 1; num_m_tiles, num_n_tiles >= 1 and their product < 2^31;
- * flags: only GEMM_SCHED_GROUPED matters (others allowed).
+ * flags: only GEMM_SCHED_GROUPED matters (others allowed). Under
+ * GEMM_SCHED_DYNAMIC the map tile_id -> (tile_m, tile_n) is this one, but
+ * which program computes a tile is decided at run time, so the program
+ * column describes the static order only.
  */
 gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles,
                                 int32_t group_size_m, uint32_t flags, int32_t grid,
