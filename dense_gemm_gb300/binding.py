@@ -3,7 +3,8 @@
 Every function here forwards to the C-ABI library ``libgemm_f16.so``; the
 arithmetic runs in its CUDA kernels. Torch is used for device memory and the
 current stream. If the library has not been built, every call raises
-``GemmError`` — there is no fallback path.
+``GemmError`` — there is no fallback path. ``GEMM_LIBRARY=debug`` selects
+``libgemm_f16_debug.so`` (device-side bounds checks, ``GEMM_ERR_CHECK``).
 """
 import ctypes
 import os
@@ -20,7 +21,7 @@ SCHED_NON_PERSISTENT = 0x8
 SCHED_DYNAMIC = 0x10
 
 _STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
-           3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT"}
+           3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT", 5: "GEMM_ERR_CHECK"}
 
 
 class GemmError(RuntimeError):
@@ -34,6 +35,8 @@ _lib = None
 
 
 def library_path() -> str:
+    if os.environ.get("GEMM_LIBRARY", "") == "debug":
+        return os.path.join(_HERE, "libgemm_f16_debug.so")
     return os.path.join(_HERE, _LIB_NAME)
 
 
@@ -45,7 +48,8 @@ def load_library():
     path = library_path()
     if not os.path.exists(path):
         raise GemmError(3, f"{path} is missing: build it with "
-                           "`python -m dense_gemm_gb300.build` (no fallback path exists)")
+                           "`python -m dense_gemm_gb300.build` (`--debug` for the checked "
+                           "library; no fallback path exists)")
     lib = ctypes.CDLL(path)
     i64, i32, u32, vp = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_void_p
     pi32 = ctypes.POINTER(ctypes.c_int32)
@@ -77,6 +81,8 @@ def load_library():
     lib.gemm_f16_set_wait_timeout.restype = ctypes.c_int
     lib.gemm_f16_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.gemm_f16_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gemm_f16_selftest_check.argtypes = [vp]
+    lib.gemm_f16_selftest_check.restype = ctypes.c_int
     lib.gemm_f16_status_str.argtypes = [ctypes.c_int]
     lib.gemm_f16_status_str.restype = ctypes.c_char_p
     _lib = lib
@@ -260,6 +266,13 @@ def kernel_info(variant: int = 0) -> dict:
 def sync_status(stream=None) -> int:
     """Synchronize and return (and clear) the device status code."""
     return int(load_library().gemm_f16_sync_status(_stream_handle(stream)))
+
+
+def selftest_check(stream=None) -> int:
+    """Debug library only: one device-side check that fails (no access behind
+    it); returns the entry point's status (GEMM_ERR_UNSUPPORTED = 2 in the
+    product library)."""
+    return int(load_library().gemm_f16_selftest_check(_stream_handle(stream)))
 
 
 def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None):

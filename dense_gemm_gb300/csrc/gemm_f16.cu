@@ -262,6 +262,7 @@ const char *gemm_f16_status_str(gemm_status_t s) {
         case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
         case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+        case GEMM_ERR_CHECK: return "GEMM_ERR_CHECK";
     }
     return "GEMM_ERR_UNKNOWN";
 }
@@ -630,12 +631,29 @@ gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t 
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+gemm_status_t gemm_f16_selftest_check(gemm_stream_t stream_) {
+#ifdef GEMM_DEBUG
+    check_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream_)>>>();
+    return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+#else
+    (void)stream_;
+    return GEMM_ERR_UNSUPPORTED;  // the product build has no device-side checks
+#endif
+}
+
 gemm_status_t gemm_f16_sync_status(gemm_stream_t stream_) {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_)) != cudaSuccess)
         return GEMM_ERR_CUDA;
     unsigned int st = 0;
     const unsigned int zero = 0;
     if (cudaMemcpyFromSymbol(&st, g_status, sizeof(st)) != cudaSuccess) return GEMM_ERR_CUDA;
+#ifdef GEMM_DEBUG
+    if (st == kStatusCheck) {
+        unsigned int line = 0;
+        if (cudaMemcpyFromSymbol(&line, g_check_line, sizeof(line)) == cudaSuccess)
+            std::fprintf(stderr, "[gemm_f16] device check failed at source line %u\n", line);
+    }
+#endif
     if (st != 0) {
         // clear the status, and the aborted launch's epoch: a CUDA graph replays a
         // launch with the epoch it was captured with

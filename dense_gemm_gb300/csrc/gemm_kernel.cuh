@@ -138,6 +138,17 @@ __device__ unsigned int g_status;
 __device__ unsigned int g_abort_epoch;
 
 constexpr unsigned int kStatusTimeout = 4;  // == GEMM_ERR_TIMEOUT
+constexpr unsigned int kStatusCheck = 5;    // == GEMM_ERR_CHECK (debug build)
+
+#ifdef GEMM_DEBUG
+// Source line of the first failed debug check (read by gemm_f16_sync_status).
+__device__ unsigned int g_check_line;
+
+__device__ __noinline__ bool check_failed(int line) {
+    if (atomicCAS(&g_status, 0u, kStatusCheck) == 0u) atomicExch(&g_check_line, unsigned(line));
+    return false;
+}
+#endif
 
 struct WaitCtl {
     uint64_t timeout_ns;
@@ -574,7 +585,8 @@ __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, i
             float *dst = p.C + row0 * p.scm + col;
 #pragma unroll
             for (int r = 0; r < 32; ++r)
-                if (r < rows) dst[r * p.scm] = __uint_as_float(v[r]);
+                if (r < rows && G16_CHECK(row0 + r >= 0 && row0 + r < p.M && col >= 0))
+                    dst[r * p.scm] = __uint_as_float(v[r]);
         }
     }
 }
@@ -638,7 +650,7 @@ __device__ __forceinline__ void store_chunk16(uint32_t (&w)[32], int64_t row0, i
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (row0 < p.M && col0 < p.N)
+            if (row0 < p.M && col0 < p.N && G16_CHECK((col0 & 7) == 0))
                 tma_store_2d_hint(tmC, stg, int32_t(col0), int32_t(row0), l2_policy_evict_first());
             bulk_commit_group();
         }
@@ -656,7 +668,7 @@ __device__ __forceinline__ void store_chunk16(uint32_t (&w)[32], int64_t row0, i
             const bool both = col + 1 < p.N;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
-                if (r < rows) {
+                if (r < rows && G16_CHECK(row0 + r >= 0 && row0 + r < p.M && col >= 0)) {
                     dst[r * p.scm] = uint16_t(w[r] & 0xffffu);
                     if (both) dst[r * p.scm + 1] = uint16_t(w[r] >> 16);
                 }
@@ -968,6 +980,14 @@ __global__ void wait_timeout_selftest_kernel(WaitCtl w) {
     mbar_wait(b, 0, w);  // phase 0 never completes
 }
 
+#ifdef GEMM_DEBUG
+// Debug-check self-test: one check that fails and guards no access, so that
+// the reporting path is exercised without any faulty access.
+__global__ void check_selftest_kernel() {
+    if (threadIdx.x == 0) (void)G16_CHECK(false);
+}
+#endif
+
 __global__ void tile_map_kernel(Sched s, int32_t num_tiles, int32_t *out) {
     if (threadIdx.x != 0) return;
     for (int32_t t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -993,6 +1013,7 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, void *__restri
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = e / nq, j = (e - i * nq) * 4;
+        if (!G16_CHECK(i < M && j < N && j + 4 <= ldw)) continue;
         const float *w = W + i * ldw + j;
         float4 acc = *reinterpret_cast<const float4 *>(w);  // ldw % 4 == 0, W 16-byte aligned
         for (int32_t s = 1; s < S; ++s) {
@@ -1036,6 +1057,7 @@ __global__ void zero_c_kernel(void *C, int64_t M, int64_t N, int64_t scm, int32_
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e - i * N;
+        if (!G16_CHECK(i < M && j < N)) continue;
         if (esize == 4)
             static_cast<float *>(C)[i * scm + j] = 0.0f;
         else

@@ -10,6 +10,27 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ---------------------------------------------------------------- debug checks
+// Debug build (GEMM_DEBUG): G16_CHECK(cond) records GEMM_ERR_CHECK and the
+// source line in the sticky status words when cond is false (no trap), and the
+// access it guards is skipped. In the product build it is the constant true and
+// compiles to nothing.
+#ifdef GEMM_DEBUG
+__device__ bool check_failed(int line);  // defined beside the status words
+#define G16_CHECK(cond) ((cond) || ::g16::check_failed(__LINE__))
+#else
+#define G16_CHECK(cond) true
+#endif
+
+// [addr, addr + bytes) lies inside this CTA's dynamic shared memory.
+__device__ __forceinline__ bool smem_window_ok(uint32_t addr, uint32_t bytes) {
+    extern __shared__ uint8_t g16_dyn_smem[];
+    uint32_t size;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+    const uint32_t lo = smem_addr(g16_dyn_smem);
+    return addr >= lo && addr + bytes <= lo + size;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -74,11 +95,13 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
 }
 
 __device__ __forceinline__ void st_shared_s32(uint32_t addr, int32_t v) {
+    if (!G16_CHECK(smem_window_ok(addr, 4))) return;
     asm volatile("st.shared.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int32_t ld_shared_s32(uint32_t addr) {
-    int32_t v;
+    int32_t v = 0;
+    if (!G16_CHECK(smem_window_ok(addr, 4))) return v;
     asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
@@ -122,8 +145,11 @@ __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// Every tensor map loaded in this library holds 16-bit elements: the innermost
+// coordinate of a copy must be a multiple of 8 (16 bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y,
                                             uint32_t bar) {
+    if (!G16_CHECK((x & 7) == 0 && smem_window_ok(dst, 16))) return;
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
@@ -131,7 +157,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// Stores start at non-negative coordinates with x on a 16-byte boundary (a
+// multiple of 4 here; 16-bit C checks its multiple of 8 where it stores).
 __device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
+    if (!G16_CHECK(x >= 0 && y >= 0 && (x & 3) == 0 && smem_window_ok(src, 16))) return;
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                      tmap),
                  "r"(x), "r"(y), "r"(src)
@@ -177,7 +206,14 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base lane + i).
+// The kernels allocate all 512 TMEM columns (base column 0).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+#ifdef GEMM_DEBUG
+    if (!__all_sync(0xffffffffu, G16_CHECK((taddr & 0xFFFFu) + 32u <= 512u))) {
+        for (int i = 0; i < 32; ++i) r[i] = 0;
+        return;
+    }
+#endif
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
@@ -198,19 +234,25 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // ---------------------------------------------------------------- shared stores
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
+    if (!G16_CHECK(smem_window_ok(addr, 16))) return;
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_shared_b32(uint32_t addr) {
-    uint32_t v;
+    uint32_t v = 0;
+    if (!G16_CHECK(smem_window_ok(addr, 4))) return v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
     return v;
 }
 
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t &a, uint32_t &b, uint32_t &c,
                                              uint32_t &d) {
+    if (!G16_CHECK(smem_window_ok(addr, 16))) {
+        a = b = c = d = 0;
+        return;
+    }
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
                  : "r"(addr)
@@ -262,6 +304,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // mbarrier that may live in the peer CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, int32_t x, int32_t y,
                                                  uint32_t bar_cluster) {
+    if (!G16_CHECK((x & 7) == 0 && smem_window_ok(dst, 16))) return;
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
@@ -309,6 +352,7 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
 
 __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *tmap, int32_t x,
                                                       int32_t y, uint32_t bar_cluster, uint64_t pol) {
+    if (!G16_CHECK((x & 7) == 0 && smem_window_ok(dst, 16))) return;
     asm volatile(
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
@@ -318,6 +362,7 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void *
 
 __device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src, int32_t x, int32_t y,
                                                   uint64_t pol) {
+    if (!G16_CHECK(x >= 0 && y >= 0 && (x & 3) == 0 && smem_window_ok(src, 16))) return;
     asm volatile(
         "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
             tmap),
@@ -396,6 +441,7 @@ namespace g16 {
 
 __device__ __forceinline__ void tma_store_3d_hint(const void *tmap, uint32_t src, int32_t x, int32_t y,
                                                   int32_t z, uint64_t pol) {
+    if (!G16_CHECK(x >= 0 && y >= 0 && z >= 0 && (x & 3) == 0 && smem_window_ok(src, 16))) return;
     asm volatile(
         "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
             tmap),

@@ -51,7 +51,10 @@ typedef enum {
     GEMM_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad stride/flag/G */
     GEMM_ERR_UNSUPPORTED = 2, /* layout the kernels do not take (see gemm_f16) */
     GEMM_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed            */
-    GEMM_ERR_TIMEOUT = 4      /* a bounded device wait ran out (kernel gave up) */
+    GEMM_ERR_TIMEOUT = 4,     /* a bounded device wait ran out (kernel gave up) */
+    GEMM_ERR_CHECK = 5        /* debug build (GEMM_DEBUG) only: a device-side bounds or
+                                 alignment check failed; the access was skipped and the
+                                 source line is printed by gemm_f16_sync_status */
 } gemm_status_t;
 
 /* schedule_flags bits */
@@ -260,7 +263,8 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
  * gemm_f16_sync_status — synchronize `stream`, then return and clear the
  * sticky device status of the current device: GEMM_ERR_TIMEOUT if any
  * kernel's bounded wait ran out since the last call (that call's C is
- * undefined), GEMM_ERR_CUDA if the synchronize failed, else GEMM_OK.
+ * undefined), GEMM_ERR_CHECK if a debug-build device check failed (the source
+ * line goes to stderr), GEMM_ERR_CUDA if the synchronize failed, else GEMM_OK.
  * Calls of the other entry points enqueue work only (no synchronisation, no
  * allocation after the first call on a device), so they can be captured in a
  * CUDA graph; a replayed launch reuses its captured abort epoch, which this
@@ -284,6 +288,15 @@ gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns);
  * gemm_f16_sync_status) and the kernel returns; the CUDA context stays usable.
  */
 gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t stream);
+
+/*
+ * gemm_f16_selftest_check — debug build (GEMM_DEBUG) only: launches one
+ * device-side check that fails without guarding any access, so that
+ * gemm_f16_sync_status then returns GEMM_ERR_CHECK (and clears it). The product
+ * build has no device-side checks and returns GEMM_ERR_UNSUPPORTED.
+ * No counterpart on the pages (it stands in for a sanitizer run).
+ */
+gemm_status_t gemm_f16_selftest_check(gemm_stream_t stream);
 
 /* gemm_f16_status_str — static, human-readable name of a status code. */
 const char *gemm_f16_status_str(gemm_status_t status);

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert "gemm_f16" in names and "gemm_f16_tile_map" in names
-    assert len(names) == 12, names
+    assert len(names) == 13, names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,6 +43,7 @@ def test_status_strings(lib):
     assert status_str(2) == "GEMM_ERR_UNSUPPORTED"
     assert status_str(3) == "GEMM_ERR_CUDA"
     assert status_str(4) == "GEMM_ERR_TIMEOUT"
+    assert status_str(5) == "GEMM_ERR_CHECK"
 
 
 def _call(lib, **kw):
@@ -103,6 +104,10 @@ def test_wait_timeout_validation(lib):
     assert lib.gemm_f16_set_wait_timeout(2_000_000_000) == 0
     assert lib.gemm_f16_selftest_wait_timeout(999, 0) == 1
     assert lib.gemm_f16_selftest_wait_timeout(10 ** 11, 0) == 1
+
+
+def test_product_library_has_no_device_checks(lib):
+    assert lib.gemm_f16_selftest_check(None) == 2  # GEMM_ERR_UNSUPPORTED
 
 
 def test_kernel_info_rejects_unknown_variant(lib):
