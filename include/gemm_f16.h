@@ -93,7 +93,9 @@ typedef enum {
  * Operands whose base address is 16-byte aligned and whose non-unit stride is
  * a multiple of 8 elements (A, B) or 4 elements (C) go through TMA; others
  * (e.g. K = 257 row-major) through a predicated load/store path with the same
- * results. On that path the rows of A and B are copied per alignment class
+ * results. C also needs N to be a multiple of 4 for TMA stores (a clipped TMA
+ * store writes whole 16-byte granules; the plain path writes exactly the M x N
+ * elements). On that path the rows of A and B are copied per alignment class
  * (rows whose start shares its offset in a 16-byte granule), from the granule
  * boundary below each row start: it may read, and discard, bytes that share
  * an aligned 16-byte granule with an element of A or B, never others. If the
@@ -136,7 +138,7 @@ gemm_status_t gemm_f16(const void *A, const void *B, float *C,
  * c_dtype (GEMM_OUT_*; unknown values -> GEMM_ERR_INVALID_ARG). Halving the
  * output bytes matters when K is small and the store dominates the traffic.
  * C: device pointer to M x N elements of c_dtype, stride_cn == 1; TMA stores
- * need a 16-byte-aligned base and stride_cm a multiple of 16 bytes, otherwise
+ * need a 16-byte-aligned base, stride_cm and N multiples of 16 bytes, otherwise
  * the predicated store path is used. K == 0 writes +0. All other arguments,
  * layouts and errors as gemm_f16; gemm_f16 equals gemm_f16_out with
  * GEMM_OUT_F32 and alpha = 1.
