@@ -520,7 +520,8 @@ def run_sweep(args):
     persistence - the pages' four variants (tiled / persistent x row-major /
                   grouped) at 8192^2 and 16384^2, K = 4096;
     cublas - context line: torch.matmul (cuBLAS, fp16 output) on 8192^2 and
-             16384^2, K = 4096, next to gemm_f16 on the same operands;
+             16384^2, K = 4096, next to gemm_f16 (fp32 C) and gemm_f16_out (fp16 C)
+             on the same operands;
     splitk - gemm_f16 vs gemm_f16_splitk (automatic slices) on 512^3 and
              1024^2 x 32768 (fewer tiles than CTA pairs);
     outdtype - fp32 vs fp16 vs bf16 C (gemm_f16_out) on the headline workload
@@ -554,7 +555,7 @@ def run_sweep(args):
         points = [dict(grouped=True, cross_tile=True, single_cta=False), "splitk"]
     elif args.sweep == "cublas":
         names = ["square_8192x8192x4096", HEADLINE]
-        points = [dict(grouped=True, cross_tile=True, single_cta=False), "torch.matmul"]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False), ("out", torch.float16), "torch.matmul"]
     elif args.sweep == "persistence":
         names = ["square_8192x8192x4096", HEADLINE]
         points = [dict(grouped=g, cross_tile=True, single_cta=False, persistent=per)
