@@ -14,6 +14,9 @@
 //     reuses an accumulator only after both epilogues have released it.
 // Per SM and 64-deep k-block this moves 32 KiB from L2 into shared memory
 // (48 KiB for the single-CTA 128 x 256 tile) for the same tensor work.
+// kDyn (TMA loads only) replaces the static pid + i*P stream by cluster launch
+// control: one cluster per unit in the grid, resident clusters cancel those that
+// have not started and take their units, in ascending order.
 // Predicated-load variant (kTmaLoad = false, operands not describable by one
 // tensor map): per CTA one warp issues the TMA copies of the alignment-class
 // boxes (see gemm_kernel.cuh) into four staging rings, and four warps each
