@@ -52,6 +52,9 @@ def parse_args(argv=None):
     p.add_argument("--group-size", type=int, default=8)
     p.add_argument("--cross-tile", choices=["on", "off"], default="on")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--e2e-repeats", type=int, default=2,
+                   help="timed e2e windows of --e2e-steps each; the fastest is reported, all are listed "
+                        "(the host link is shared with the rest of the machine)")
     p.add_argument("--burst-launches", type=int, default=10,
                    help="launches of the short burst loop after the timed region (0: skip)")
     p.add_argument("--no-e2e", action="store_true")
@@ -430,21 +433,25 @@ def run_gpu(args, w):
         for _ in range(2):  # warm-up: both buffer sets
             pipe.submit(A_pin, B_pin, C_pin)
         pipe.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if world > 1:
-            dist.barrier()
-        e0.record(pipe.s_in)
-        for _ in range(args.e2e_steps):
-            pipe.submit(A_pin, B_pin, C_pin)
-        e1.record(pipe.s_out)
-        pipe.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        windows = []
+        for _ in range(max(1, args.e2e_repeats)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if world > 1:
+                dist.barrier()
+            e0.record(pipe.s_in)
+            for _ in range(args.e2e_steps):
+                pipe.submit(A_pin, B_pin, C_pin)
+            e1.record(pipe.s_out)
+            pipe.synchronize()
+            windows.append(max_over_ranks(e0.elapsed_time(e1), dev))
+        e2e_ms = min(windows)
         e2e = {"value": job_throughput(world, flops, args.e2e_steps, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_bytes,
                "link_gbs": link,
                # uploads and downloads of consecutive steps overlap: the slower direction bounds a step
                "link_bound_ms_per_step": max(in_bytes / link["h2d"], out_bytes / link["d2h"]) / 1e6,
                "steps": args.e2e_steps, "ms_per_step": e2e_ms / args.e2e_steps,
+               "windows_ms_per_step": [x / args.e2e_steps for x in windows],
                "api": "dense_gemm_gb300.HostPipeline (pinned host A, B -> device, gemm_f16, "
                       "C -> pinned host; upload+GEMM of step i+1 overlap the download of step i)"}
         del pipe, A_pin, B_pin, C_pin
