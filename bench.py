@@ -31,8 +31,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-NOMINAL_FP16_TFLOPS = 2250.0        # nominal dense bf16/fp16 tensor peak per GPU
-NVL72_SPEC_FP16_TFLOPS = 2500.0     # GB300 NVL72 dense fp16 (360 PF sparse / 72 / 2)
+# P of the target: GB300 dense FP16 tensor peak per GPU, from the GB300 NVL72
+# specification (360 PFLOP/s sparse FP16 for 72 GPUs, halved for dense).
+SPEC_FP16_TFLOPS = 2500.0
+TARGET_FRACTION = 0.70              # the headline goal: >= 70 % of P
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -168,6 +170,41 @@ class ClockSampler:
                 "reasons": reasons,
                 "power_w_max": max(power) if power else None,
                 "samples": len(inside), "samples_near": len(used) - len(inside)}
+
+
+def power_capped(clocks):
+    """Did the clock samples of the timed loop show it running at the power
+    limit (sw_power_cap active, or a median SM clock below 90 % of its max)?"""
+    if not clocks:
+        return False, "no clock samples"
+    if "sw_power_cap" in clocks.get("reasons", []):
+        return True, "the clock samples of the timed loop show sw_power_cap"
+    mhz, top = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    if mhz and top and mhz < 0.9 * top:
+        return True, f"the median SM clock of the timed loop ({mhz:g} MHz) is below 90 % of its max ({top:g})"
+    return False, "the clock samples of the timed loop show neither sw_power_cap nor a lowered SM clock"
+
+
+def roofline_peak(peaks, source, clocks):
+    """(peak TFLOP/s, note): the measured cuBLAS bf16 peak for the regime the
+    timed loop ran in: the sustained one when it ran at the power limit, else
+    the burst one (fp16 and bf16 have the same nominal dense rate)."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
+    capped, why = power_capped(clocks)
+    regime = "sustained" if capped and sustained else "burst"
+    peak = sustained if regime == "sustained" else burst
+    return peak, (f"{source} cuBLAS bf16 {regime} peak (MEASURED_PEAKS.json) x nominal fp16/bf16 "
+                  f"ratio 1.0; {regime} because {why}")
+
+
+def target_line(value_per_gpu, bound_tflops):
+    """The headline goal, stated on one P: the GB300 dense FP16 tensor peak."""
+    return {"P_tflops": SPEC_FP16_TFLOPS,
+            "P_source": "GB300 NVL72 specification: 360 PFLOP/s sparse FP16 / 72 GPUs / 2 (dense)",
+            "frac_of_P": value_per_gpu / SPEC_FP16_TFLOPS, "goal_frac": TARGET_FRACTION,
+            "met": value_per_gpu >= TARGET_FRACTION * SPEC_FP16_TFLOPS,
+            "frac_of_min_P_BWxI": value_per_gpu / bound_tflops}
 
 
 def dist_env():
@@ -370,7 +407,7 @@ def run_gpu(args, w):
         props = torch.cuda.get_device_properties(dev)
         gpu_id = getattr(props, "uuid", None)
         gpu_id = f"GPU-{gpu_id}" if gpu_id is not None and not str(gpu_id).startswith("GPU-") else gpu_id
-        sampler = ClockSampler(gpu_id)
+        sampler = ClockSampler(gpu_id, period_ms=20)
         time.sleep(0.6)   # let nvidia-smi start
         for _ in range(max(args.warmup, 3)):
             step()
@@ -462,15 +499,12 @@ def run_gpu(args, w):
         return 0
 
     peaks, peak_src = load_peaks()
+    peak, peak_note = roofline_peak(peaks, peak_src, clocks)
     burst_peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-    # the timed loop is hundreds of back-to-back launches at the power limit:
-    # compare it with the sustained peak (the burst one when there is none)
-    sustained = float(peaks.get("bf16_tflops_sustained", 0.0)) or None
-    peak = sustained or burst_peak
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     compulsory = 2 * (w.M * w.K + w.K * w.N) + 4 * w.M * w.N
     intensity = flops / compulsory
-    bound_tflops = min(NVL72_SPEC_FP16_TFLOPS, hbm * 1e9 * intensity / 1e12)
+    bound_tflops = min(SPEC_FP16_TFLOPS, hbm * 1e9 * intensity / 1e12)
     traffic = recorded_traffic(w.name, args.order, cross)
     info = kernel_info(0 if args.single_cta else 4)
 
@@ -483,14 +517,9 @@ def run_gpu(args, w):
                                             "accumulate": "f32", "output": "f32",
                                             "tiles": "one CTA, 128x256" if args.single_cta
                                             else "CTA pair (cta_group::2), 256x256"}),
-        "pct_of_peak": {"nvl72_spec_2500": 100.0 * value / world / NVL72_SPEC_FP16_TFLOPS,
-                        "nominal_2250": 100.0 * value / world / NOMINAL_FP16_TFLOPS,
-                        f"{peak_src}_bf16_burst_{burst_peak:g}": 100.0 * value / world / burst_peak},
+        "target": target_line(value / world, bound_tflops),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": (f"{peak_src} cuBLAS bf16 {'sustained' if sustained else 'burst'} "
-                                     "(MEASURED_PEAKS.json) x nominal fp16/bf16 ratio 1.0; the timed "
-                                     "loop runs at the power limit"),
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
                      "burst": ({"achieved": flops / (burst_ms * 1e-3) / 1e12, "peak": burst_peak,
                                 "frac": flops / (burst_ms * 1e-3) / 1e12 / burst_peak,
                                 "launches": args.burst_launches, "avg_launch_ms": burst_ms,

@@ -94,10 +94,22 @@ def _check(status: int, what: str):
         raise GemmError(status, what)
 
 
-def _stream_handle(stream=None) -> int:
+def _stream_handle(stream=None, device=None) -> int:
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
     return int(stream.cuda_stream)
+
+
+def _common_device(*tensors) -> torch.device:
+    """The one CUDA device all `tensors` live on. The C entry points work on the
+    current device (its status words, its scratch and its stream), so every
+    call is made with this device current."""
+    devs = {t.device for t in tensors}
+    if len(devs) != 1:
+        raise ValueError(f"A, B and out must be on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
 
 
 def status_str(status: int) -> str:
@@ -147,21 +159,23 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     if out.dtype not in _OUT_CODES or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32/float16/bfloat16 CUDA tensor of shape [M, N]")
+    dev = _common_device(A, B, out)
     flags = sched_flags(grouped, cross_tile, single_cta, persistent, dynamic)
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
     # torch gives stride 1 to size-1 dims' neighbours freely; keep them >= 1
     strides = (max(sam, 1), max(sak, 1), max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1))
-    if out.dtype == torch.float32 and alpha == 1.0:
-        st = gemm_raw(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, *strides,
-                      group_size_m, flags, _stream_handle(stream))
-        _check(st, "gemm_f16")
-    else:
-        st = load_library().gemm_f16_out(A.data_ptr(), B.data_ptr(), out.data_ptr(),
-                                         _OUT_CODES[out.dtype], float(alpha), M, N, K, *strides,
-                                         group_size_m, flags, _stream_handle(stream))
-        _check(st, "gemm_f16_out")
+    with torch.cuda.device(dev):
+        if out.dtype == torch.float32 and alpha == 1.0:
+            st = gemm_raw(A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, *strides,
+                          group_size_m, flags, _stream_handle(stream, dev))
+            _check(st, "gemm_f16")
+        else:
+            st = load_library().gemm_f16_out(A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                                             _OUT_CODES[out.dtype], float(alpha), M, N, K, *strides,
+                                             group_size_m, flags, _stream_handle(stream, dev))
+            _check(st, "gemm_f16_out")
     return out
 
 
@@ -177,6 +191,7 @@ def _check_operands(A, B, out):
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     if out.dtype != torch.float32 or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32 CUDA tensor of shape [M, N]")
+    _common_device(A, B, out)
     return out
 
 
@@ -198,17 +213,20 @@ def gemm_splitk(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *, s
     out = _check_operands(A, B, out)
     M, K = A.shape
     N = B.shape[1]
-    need, _ = splitk_workspace_size(M, N, K, splits)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=A.device)
-    ws_bytes = workspace.numel() * workspace.element_size()
-    sam, sak = A.stride()
-    sbk, sbn = B.stride()
-    scm, scn = out.stride()
-    st = load_library().gemm_f16_splitk(
-        A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1), max(sbk, 1),
-        max(sbn, 1), max(scm, 1), max(scn, 1), splits, workspace.data_ptr(), ws_bytes, group_size_m,
-        sched_flags(grouped, cross_tile), _stream_handle(stream))
+    dev = A.device
+    with torch.cuda.device(dev):
+        need, _ = splitk_workspace_size(M, N, K, splits)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        _common_device(A, workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        sam, sak = A.stride()
+        sbk, sbn = B.stride()
+        scm, scn = out.stride()
+        st = load_library().gemm_f16_splitk(
+            A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1), max(sbk, 1),
+            max(sbn, 1), max(scm, 1), max(scn, 1), splits, workspace.data_ptr(), ws_bytes, group_size_m,
+            sched_flags(grouped, cross_tile), _stream_handle(stream, dev))
     _check(st, "gemm_f16_splitk")
     return out
 
@@ -225,10 +243,12 @@ def gemm_splitk_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, *, 
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
-    st = load_library().gemm_f16_splitk_noalloc(
-        A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1),
-        max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1), splits, group_size_m,
-        sched_flags(grouped, cross_tile), _stream_handle(stream))
+    dev = A.device
+    with torch.cuda.device(dev):  # the entry point uses the current device's scratch
+        st = load_library().gemm_f16_splitk_noalloc(
+            A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, max(sam, 1), max(sak, 1),
+            max(sbk, 1), max(sbn, 1), max(scm, 1), max(scn, 1), splits, group_size_m,
+            sched_flags(grouped, cross_tile), _stream_handle(stream, dev))
     _check(st, "gemm_f16_splitk_noalloc")
     return out
 
@@ -239,9 +259,10 @@ def tile_map(num_m_tiles: int, num_n_tiles: int, group_size_m: int, grouped: boo
     (program id, tile_m, tile_n)."""
     device = device or torch.device("cuda")
     out = torch.full((num_m_tiles * num_n_tiles, 3), -1, dtype=torch.int32, device=device)
-    st = load_library().gemm_f16_tile_map(num_m_tiles, num_n_tiles, group_size_m,
-                                          SCHED_GROUPED if grouped else 0, grid,
-                                          out.data_ptr(), _stream_handle(stream))
+    with torch.cuda.device(out.device):
+        st = load_library().gemm_f16_tile_map(num_m_tiles, num_n_tiles, group_size_m,
+                                              SCHED_GROUPED if grouped else 0, grid,
+                                              out.data_ptr(), _stream_handle(stream, out.device))
     _check(st, "gemm_f16_tile_map")
     return out
 

@@ -25,9 +25,11 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<uint32_t> g_epoch{0};
 
+// Per-device set-up, done by the first call on a device that succeeds; a call
+// whose set-up fails returns the error and the next call tries again.
 struct DeviceState {
-    std::once_flag once;
-    cudaError_t init_err = cudaSuccess;
+    std::mutex mu;
+    std::atomic<bool> ready{false};
     int num_sms = 0;
     int max_pairs = 0;       // co-resident 2-CTA clusters of the pair kernel (TMA loads)
     int max_pairs_pred = 0;  // the same for its predicated-load variant
@@ -87,24 +89,31 @@ int query_max_pairs(int num_sms) {
 cudaError_t device_init(int dev, DeviceState **out) {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     DeviceState &d = g_dev[dev];
-    std::call_once(d.once, [&d, dev] {
-        cudaError_t e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess) e = set_smem_attr<true, true>();
-        if (e == cudaSuccess) e = set_smem_attr<true, false>();
-        if (e == cudaSuccess) e = set_smem_attr<false, true>();
-        if (e == cudaSuccess) e = set_smem_attr<false, false>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<true, true>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<true, false>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<false, true>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<false, false>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<true, true, true>();
-        if (e == cudaSuccess) e = set_pair_smem_attr<true, false, true>();
-        if (e == cudaSuccess) d.max_pairs = query_max_pairs<true>(d.num_sms);
-        if (e == cudaSuccess) d.max_pairs_pred = query_max_pairs<false>(d.num_sms);
-        d.init_err = e;
-    });
     *out = &d;
-    return d.init_err;
+    if (d.ready.load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(d.mu);
+    if (d.ready.load(std::memory_order_relaxed)) return cudaSuccess;
+    int num_sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = set_smem_attr<true, true>();
+    if (e == cudaSuccess) e = set_smem_attr<true, false>();
+    if (e == cudaSuccess) e = set_smem_attr<false, true>();
+    if (e == cudaSuccess) e = set_smem_attr<false, false>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, false>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<false, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<false, false>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, true, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, false, true>();
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // not sticky: leave no error behind for the caller's next call
+        return e;
+    }
+    d.num_sms = num_sms;
+    d.max_pairs = query_max_pairs<true>(num_sms);
+    d.max_pairs_pred = query_max_pairs<false>(num_sms);
+    d.ready.store(true, std::memory_order_release);
+    return cudaSuccess;
 }
 
 EncodeTiledFn encode_fn() {
@@ -679,12 +688,29 @@ constexpr uint64_t kNoAllocScratchBytes = 32ull << 20;  // 32 MiB, held by every
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The scratch array's device address on each device. Only a successful lookup
+// is kept: a lookup that fails (say, during a stream capture, or with an error
+// left over from earlier work) returns GEMM_ERR_CUDA and the next call retries.
 struct ScratchState {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    void *ptr = nullptr;
+    std::mutex mu;
+    std::atomic<void *> ptr{nullptr};
 };
 ScratchState g_scratch[kMaxDevices];
+
+void *scratch_address(int dev) {
+    ScratchState &s = g_scratch[dev];
+    void *p = s.ptr.load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+    std::lock_guard<std::mutex> lock(s.mu);
+    p = s.ptr.load(std::memory_order_relaxed);
+    if (p != nullptr) return p;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    s.ptr.store(p, std::memory_order_release);
+    return p;
+}
 
 }  // namespace
 
@@ -703,13 +729,11 @@ extern "C" gemm_status_t gemm_f16_splitk_noalloc(const void *A, const void *B, f
     void *ws = nullptr;
     if (need > 0) {
         // In host code the array's name is only a stand-in: its device address is
-        // looked up once per device, with that device current.
+        // looked up with the device current, and kept once a lookup succeeds.
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
-        ScratchState &s = g_scratch[dev];
-        std::call_once(s.once, [&s] { s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch); });
-        if (s.err != cudaSuccess || s.ptr == nullptr) return GEMM_ERR_CUDA;
-        ws = s.ptr;
+        ws = scratch_address(dev);
+        if (ws == nullptr) return GEMM_ERR_CUDA;
     }
     return gemm_f16_splitk(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm,
                            stride_cn, splits, ws, kNoAllocScratchBytes, group_size_m, schedule_flags,

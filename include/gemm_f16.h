@@ -203,7 +203,8 @@ gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, in
  *   32 MiB are rejected with GEMM_ERR_UNSUPPORTED; nothing is launched.
  * - The first call on a device that needs the scratch looks up the array's
  *   device address (cudaGetSymbolAddress) with that device current; make that
- *   first call before any stream capture.
+ *   first call before any stream capture. Only a lookup that succeeds is kept:
+ *   if it fails, the call returns GEMM_ERR_CUDA and the next call tries again.
  * - All calls share the one array and it keeps the last call's contents;
  *   nothing in it needs to start at zero. Calls that overlap on the GPU (on
  *   different streams, or from different threads) race on it: serialise them.
@@ -239,7 +240,12 @@ gemm_status_t gemm_f16_tile_map(int32_t num_m_tiles, int32_t num_n_tiles,
 /*
  * gemm_f16_get_config — tile shape and launch size gemm_f16 uses for an M x N
  * output with TMA-loadable operands and these schedule_flags, on the current
- * device. Any output pointer may be NULL; unknown flag bits -> INVALID_ARG.
+ * device. The grid rule is [persistent] "naive persistent matmul" (grid =
+ * min(#SMs, #tiles), here min(co-resident programs, #tiles)); the tile and K
+ * step stand in for the pages' BLOCK_SIZE_M/N/K and num_stages meta-parameters.
+ * It takes M, N and the flags because the grid depends on them (the pages
+ * compute the grid from the problem size in the launcher).
+ * Any output pointer may be NULL; unknown flag bits -> INVALID_ARG.
  * bm, bn, bk: output tile (256x256 per CTA pair, or 128x256 per CTA with
  * GEMM_SCHED_SINGLE_CTA) and K step; stages: shared-memory ring depth; grid:
  * persistent programs (CTA pairs or CTAs) = min(co-resident programs,
@@ -251,7 +257,9 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags,
 
 /*
  * gemm_f16_kernel_info — compiled resource use of a kernel variant
- * (cudaFuncGetAttributes). One-CTA tiles: variant 0 = TMA loads + TMA store,
+ * (cudaFuncGetAttributes). The pages print the same figures (registers, shared
+ * memory) from Triton's kernel metadata ([persistent] "Block Limit 값 직접
+ * 계산해보기"); as an entry point it has no counterpart there. One-CTA tiles: variant 0 = TMA loads + TMA store,
  * 1 = TMA loads + predicated store, 2 = predicated loads + TMA store,
  * 3 = predicated loads + predicated store. CTA-pair tiles, in the same
  * order: 4, 5, 6, 7; with GEMM_SCHED_DYNAMIC (TMA loads): 8 = TMA store,
@@ -262,7 +270,8 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *threads_per_cta);
 
 /*
- * gemm_f16_sync_status — synchronize `stream`, then return and clear the
+ * gemm_f16_sync_status — no counterpart on the pages (they describe no
+ * failure handling). Synchronize `stream`, then return and clear the
  * sticky device status of the current device: GEMM_ERR_TIMEOUT if any
  * kernel's bounded wait ran out since the last call (that call's C is
  * undefined), GEMM_ERR_CHECK if a debug-build device check failed (the source
@@ -275,8 +284,9 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
 gemm_status_t gemm_f16_sync_status(gemm_stream_t stream);
 
 /*
- * gemm_f16_set_wait_timeout — upper bound, in nanoseconds of GPU global
- * time, on any single wait inside the kernels (default 2e9 = 2 s). Applies
+ * gemm_f16_set_wait_timeout — no counterpart on the pages. Upper bound, in
+ * nanoseconds of GPU global time, on any single wait inside the kernels
+ * (default 2e9 = 2 s). Applies
  * to launches enqueued after the call. ns must be >= 1000.
  */
 gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns);
@@ -300,7 +310,8 @@ gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t 
  */
 gemm_status_t gemm_f16_selftest_check(gemm_stream_t stream);
 
-/* gemm_f16_status_str — static, human-readable name of a status code. */
+/* gemm_f16_status_str — static, human-readable name of a status code (no
+ * counterpart on the pages). Unknown codes give "GEMM_ERR_UNKNOWN". */
 const char *gemm_f16_status_str(gemm_status_t status);
 
 #ifdef __cplusplus

@@ -159,3 +159,15 @@ def test_out_dtype_validation(lib):
     assert lib.gemm_f16_out(*args, 3, C.c_float(1.0), 4, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 1
     assert lib.gemm_f16_out(*args, -1, C.c_float(1.0), 4, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 1
     assert lib.gemm_f16_out(*args, 1, C.c_float(2.0), 0, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None) == 0
+
+
+def test_binding_rejects_operands_on_different_devices():
+    """The C entry points act on the current device (status words, scratch,
+    stream); the binding therefore requires A, B and out on one device and makes
+    the call with that device current."""
+    import torch
+    from dense_gemm_gb300.binding import _common_device
+    a = torch.empty(2, 2, dtype=torch.float16)
+    assert _common_device(a, a, torch.empty(2, 2)) == torch.device("cpu")
+    with pytest.raises(ValueError, match="one CUDA device"):
+        _common_device(a, torch.empty(2, 2, dtype=torch.float16, device="meta"), a)

@@ -57,3 +57,25 @@ def test_sweeps_parse(sweep):
 def test_defaults_finish_within_minutes():
     a = bench.parse_args([])
     assert a.gpus == 1 and a.warmup >= 3 and 1 <= a.steps <= 1000
+
+
+def test_roofline_peak_follows_the_observed_regime():
+    peaks = {"bf16_tflops": 1914.3, "bf16_tflops_sustained": 1748.8}
+    unthrottled = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    peak, note = bench.roofline_peak(peaks, "measured", unthrottled)
+    assert peak == 1914.3 and "burst" in note
+    capped = {"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    peak, note = bench.roofline_peak(peaks, "measured", capped)
+    assert peak == 1748.8 and "sustained" in note and "sw_power_cap" in note
+    low = {"sm_mhz": 1500.0, "sm_max_mhz": 2070.0, "reasons": []}
+    assert bench.roofline_peak(peaks, "measured", low)[0] == 1748.8
+    # without a sustained figure, or without clock samples: the burst peak
+    assert bench.roofline_peak({"bf16_tflops": 1914.3}, "measured", capped)[0] == 1914.3
+    assert bench.roofline_peak(peaks, "measured", None)[0] == 1914.3
+
+
+def test_target_is_stated_on_one_P():
+    t = bench.target_line(1777.0, 2500.0)
+    assert t["P_tflops"] == 2500.0 and t["goal_frac"] == 0.70
+    assert abs(t["frac_of_P"] - 1777.0 / 2500.0) < 1e-12 and t["met"] is True
+    assert bench.target_line(1737.7, 2500.0)["met"] is False
