@@ -67,7 +67,7 @@ def parse_args(argv=None):
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
     p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
-                                       "outdtype", "ragged", "schedule"],
+                                       "outdtype", "ragged", "schedule", "tail"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
     return p.parse_args(argv)
@@ -565,7 +565,9 @@ def run_sweep(args):
     ragged - the two ragged workloads (4000 x 5000 x 3000 through TMA, 8191^2 x 257
              with 514-byte rows through the predicated-load path) and 512^3;
     schedule - the static pid + i*P tile stream vs GEMM_SCHED_DYNAMIC (cluster
-               launch control) on 8192^2 x 4096, 16384^2 x 1024, 4000 x 5000 x 3000."""
+               launch control) on 8192^2 x 4096, 16384^2 x 1024, 4000 x 5000 x 3000;
+    tail - GEMM_SCHED_TAIL_SPLIT off/on (fp32 C, and fp16 C) with cuBLAS (fp16 C)
+           beside, on 8192^2 x 4096, 4000 x 5000 x 3000, 512^3 and the headline."""
     import torch
     from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
@@ -583,6 +585,10 @@ def run_sweep(args):
     elif args.sweep == "schedule":
         names = ["square_8192x8192x4096", "ksweep_16384x16384x1024", "ragged_4000x5000x3000"]
         points = [dict(grouped=True, cross_tile=True, single_cta=False, dynamic=d) for d in (False, True)]
+    elif args.sweep == "tail":
+        names = ["square_8192x8192x4096", "ragged_4000x5000x3000", "square_512", HEADLINE]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False, tail_split=t) for t in (False, True)]
+        points += [("out", torch.float16), ("out16_tail", torch.float16), "torch.matmul"]
     elif args.sweep == "outdtype":
         names = [HEADLINE, "ksweep_16384x16384x512"]
         points = [("out", torch.float32), ("out", torch.float16), ("out", torch.bfloat16)]
@@ -606,7 +612,11 @@ def run_sweep(args):
         A, B = A_host.to(dev), B_host.to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
         for pt in points:
-            if isinstance(pt, tuple) and pt[0] == "out":
+            if isinstance(pt, tuple) and pt[0] == "out16_tail":
+                Cx = torch.empty((w.M, w.N), dtype=pt[1], device=dev)
+                run = lambda: gemm(A, B, Cx, group_size_m=args.group_size, tail_split=True)  # noqa: E731
+                desc = {"impl": "gemm_f16_out", "c_dtype": str(pt[1]).replace("torch.", ""), "tail_split": True}
+            elif isinstance(pt, tuple) and pt[0] == "out":
                 Cx = torch.empty((w.M, w.N), dtype=pt[1], device=dev)
                 run = lambda: gemm(A, B, Cx, group_size_m=args.group_size)  # noqa: E731
                 desc = {"impl": "gemm_f16_out" if pt[1] != torch.float32 else "gemm_f16",

@@ -19,6 +19,7 @@ SCHED_CROSS_TILE = 0x2
 SCHED_SINGLE_CTA = 0x4
 SCHED_NON_PERSISTENT = 0x8
 SCHED_DYNAMIC = 0x10
+SCHED_TAIL_SPLIT = 0x20
 
 _STATUS = {0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED",
            3: "GEMM_ERR_CUDA", 4: "GEMM_ERR_TIMEOUT", 5: "GEMM_ERR_CHECK"}
@@ -81,6 +82,8 @@ def load_library():
     lib.gemm_f16_set_wait_timeout.restype = ctypes.c_int
     lib.gemm_f16_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.gemm_f16_selftest_wait_timeout.restype = ctypes.c_int
+    lib.gemm_f16_selftest_pair_abort.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp]
+    lib.gemm_f16_selftest_pair_abort.restype = ctypes.c_int
     lib.gemm_f16_selftest_check.argtypes = [vp]
     lib.gemm_f16_selftest_check.restype = ctypes.c_int
     lib.gemm_f16_status_str.argtypes = [ctypes.c_int]
@@ -127,10 +130,10 @@ def gemm_raw(A_ptr: int, B_ptr: int, C_ptr: int, M: int, N: int, K: int,
 
 
 def sched_flags(grouped: bool = True, cross_tile: bool = True, single_cta: bool = False,
-                persistent: bool = True, dynamic: bool = False) -> int:
+                persistent: bool = True, dynamic: bool = False, tail_split: bool = False) -> int:
     return ((SCHED_GROUPED if grouped else 0) | (SCHED_CROSS_TILE if cross_tile else 0)
             | (SCHED_SINGLE_CTA if single_cta else 0) | (0 if persistent else SCHED_NON_PERSISTENT)
-            | (SCHED_DYNAMIC if dynamic else 0))
+            | (SCHED_DYNAMIC if dynamic else 0) | (SCHED_TAIL_SPLIT if tail_split else 0))
 
 
 _OUT_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
@@ -138,9 +141,13 @@ _OUT_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
          group_size_m: int = 8, grouped: bool = True, cross_tile: bool = True,
-         single_cta: bool = False, persistent: bool = True, dynamic: bool = False, alpha: float = 1.0,
+         single_cta: bool = False, persistent: bool = True, dynamic: bool = False,
+         tail_split: bool = False, alpha: float = 1.0,
          out_dtype: torch.dtype = torch.float32, stream=None) -> torch.Tensor:
     """C = alpha * (A @ B) with A [M,K], B [K,N] fp16 CUDA tensors.
+
+    The keywords map to the GEMM_SCHED_* flags (``tail_split`` to
+    GEMM_SCHED_TAIL_SPLIT).
 
     ``out`` ([M,N], unit column stride, float32 / float16 / bfloat16) is
     written if given, else allocated with ``out_dtype``. fp32 output with
@@ -160,7 +167,7 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
     if out.dtype not in _OUT_CODES or tuple(out.shape) != (M, N) or not out.is_cuda:
         raise ValueError("out must be a float32/float16/bfloat16 CUDA tensor of shape [M, N]")
     dev = _common_device(A, B, out)
-    flags = sched_flags(grouped, cross_tile, single_cta, persistent, dynamic)
+    flags = sched_flags(grouped, cross_tile, single_cta, persistent, dynamic, tail_split)
     sam, sak = A.stride()
     sbk, sbn = B.stride()
     scm, scn = out.stride()
@@ -300,6 +307,20 @@ def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None):
     """Enqueue the bounded-wait self-test kernel (see the header)."""
     _check(load_library().gemm_f16_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)),
            "gemm_f16_selftest_wait_timeout")
+
+
+def selftest_pair_abort(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, stop_after: int, stream=None):
+    """Enqueue the CTA-pair abort self-test (see the header): row-major fp16 A,
+    B and fp32 C on one device; the kernel's wait runs out and it returns."""
+    dev = _common_device(A, B, C)
+    M, K = A.shape
+    N = B.shape[1]
+    if not (A.is_contiguous() and B.is_contiguous() and C.is_contiguous()):
+        raise ValueError("the abort self-test takes contiguous row-major A, B and C")
+    with torch.cuda.device(dev):
+        _check(load_library().gemm_f16_selftest_pair_abort(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                                           int(stop_after), _stream_handle(stream, dev)),
+               "gemm_f16_selftest_pair_abort")
 
 
 def set_wait_timeout(ns: int):

@@ -57,9 +57,9 @@ cudaError_t set_smem_attr() {
                                 Layout<L>::smem_bytes);
 }
 
-template <bool L, bool S, bool D = false>
+template <bool L, bool S, bool D = false, bool T = false>
 cudaError_t set_pair_smem_attr() {
-    return cudaFuncSetAttribute(gemm_f16_pair<L, S, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_f16_pair<L, S, D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 pair::Layout<L>::smem_bytes);
 }
 
@@ -105,6 +105,7 @@ cudaError_t device_init(int dev, DeviceState **out) {
     if (e == cudaSuccess) e = set_pair_smem_attr<false, false>();
     if (e == cudaSuccess) e = set_pair_smem_attr<true, true, true>();
     if (e == cudaSuccess) e = set_pair_smem_attr<true, false, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, true, false, true>();
     if (e != cudaSuccess) {
         (void)cudaGetLastError();  // not sticky: leave no error behind for the caller's next call
         return e;
@@ -213,14 +214,14 @@ cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap
     return cudaGetLastError();
 }
 
-template <bool L, bool S, bool D = false>
-cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
-                        const ClassMaps &cm, int grid, cudaStream_t stream) {
+template <bool L, bool S, bool D = false, bool T = false>
+cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const CUtensorMap &w,
+                        const Params &p, const ClassMaps &cm, int grid, cudaStream_t stream) {
     constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
     if constexpr (L)
-        gemm_f16_pair<L, S, D><<<grid, threads, smem, stream>>>(a, b, c, p, NoClassMaps{});
+        gemm_f16_pair<L, S, D, T><<<grid, threads, smem, stream>>>(a, b, c, w, p, NoClassMaps{});
     else
-        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, p, cm);
+        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, w, p, cm);
     return cudaGetLastError();
 }
 
@@ -252,6 +253,72 @@ SplitPlan plan_splits(int64_t M, int64_t N, int64_t K, int32_t requested, int ma
     sp.splits = int32_t(cdiv(num_kb, sp.kb_per_split));
     sp.ldw = (N + 3) / 4 * 4;
     return sp;
+}
+
+// Device address of a file-scope __device__ array on the current device. In
+// host code the array's name is only a stand-in, so the address is looked up
+// with the device current, and kept only once a lookup succeeds (a failed one,
+// say during a stream capture, returns nullptr and the next call retries).
+struct SymbolAddress {
+    std::mutex mu;
+    std::atomic<void *> ptr{nullptr};
+};
+
+template <typename T>
+void *symbol_address(SymbolAddress &s, const T &symbol) {
+    void *p = s.ptr.load(std::memory_order_acquire);
+    if (p != nullptr) return p;
+    std::lock_guard<std::mutex> lock(s.mu);
+    p = s.ptr.load(std::memory_order_relaxed);
+    if (p != nullptr) return p;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    s.ptr.store(p, std::memory_order_release);
+    return p;
+}
+
+// Split tail (GEMM_SCHED_TAIL_SPLIT): scratch for the fp32 partial tiles of a
+// split last round, built into the library (every GPU that loads it holds it).
+constexpr uint64_t kTailScratchBytes = 24ull << 20;
+constexpr uint64_t kTailTileBytes = uint64_t(pair::TILE_M) * pair::TILE_N * 4;  // 256 KiB
+constexpr int64_t kTailSlots = int64_t(kTailScratchBytes / kTailTileBytes);     // 96 partial tiles
+static __device__ __align__(256) unsigned char g_tail_scratch[kTailScratchBytes];
+SymbolAddress g_tail_addr[kMaxDevices];
+
+struct TailPlan {
+    int32_t first = 0, tiles = 0, splits = 1, kps = 0;
+};
+
+// The last round of the static tile stream tile_id = pid + i * P, when it
+// would leave at least three quarters of the P programs idle: its tiles are
+// split along K into as many slices (at least two) as the idle programs and
+// the scratch allow, each of at least kTailMinKb k-blocks, so that the round
+// takes a fraction of a tile's time. Measured on GB300 (device-timed loops):
+// 4000 x 5000 x 3000 (16 tiles of 76 in the last round) 108.8 -> 105.6 us;
+// with a fuller last round (8192^2 x 4096: 36 of 76) the second pass cost more
+// than it saved (320 -> 326 us), since the SMs that sit out a partial round let
+// the busy ones clock higher under the power limit; for short problems (512^3)
+// the second launch dominates.
+constexpr int64_t kTailMinKb = 8;
+
+TailPlan plan_tail(int64_t num_tiles, int64_t num_kb, int64_t programs) {
+    TailPlan t;
+    const int64_t rest = num_tiles % programs;
+    if (rest == 0 || 4 * rest > programs) return t;
+    int64_t S = programs / rest;
+    if (S > kTailSlots / rest) S = kTailSlots / rest;
+    if (S > num_kb / kTailMinKb) S = num_kb / kTailMinKb;
+    if (S < 2) return t;
+    const int64_t kps = cdiv(num_kb, S);
+    S = cdiv(num_kb, kps);  // no empty slice
+    if (S < 2) return t;
+    t.first = int32_t(num_tiles - rest);
+    t.tiles = int32_t(rest);
+    t.splits = int32_t(S);
+    t.kps = int32_t(kps);
+    return t;
 }
 
 uint32_t next_epoch() {
@@ -293,6 +360,7 @@ struct SplitReq {
     int32_t splits = 1;
     void *workspace = nullptr;
     uint64_t workspace_bytes = 0;
+    int32_t stop_after = 0;  // failure-detection self-test (gemm_f16_selftest_pair_abort)
 };
 
 gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -354,10 +422,11 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     const int64_t nm = cdiv(M, tile_m), nn = cdiv(N, tile_n);
     if (nm * nn > kMaxDim) return GEMM_ERR_UNSUPPORTED;
 
-    CUtensorMap tmA, tmB, tmC;
+    CUtensorMap tmA, tmB, tmC, tmW;
     std::memset(&tmA, 0, sizeof(tmA));
     std::memset(&tmB, 0, sizeof(tmB));
     std::memset(&tmC, 0, sizeof(tmC));
+    std::memset(&tmW, 0, sizeof(tmW));
     if (load_tma) {
         const bool okA = a_k ? encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, stride_am * 2, BK,
                                          cta_m)
@@ -452,6 +521,7 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     p.l2_mode = 1u;
     p.wait.timeout_ns = g_timeout_ns.load();
     p.wait.epoch = next_epoch();
+    p.stop_after = sk.stop_after;
 
     // dynamic units: one cluster per unit in the grid; the resident clusters take
     // the others' units through cluster launch control (CTA pairs with TMA loads)
@@ -461,24 +531,44 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     const int programs = !persistent ? p.num_units
                          : use_pair  ? (load_tma ? ds->max_pairs : ds->max_pairs_pred)
                                      : ds->num_sms;
+    p.tail_first = p.num_units;  // no split tail
+    p.tail_tiles = 1;
+    p.tail_kps = p.num_kb;
+    TailPlan tp;
+    if ((schedule_flags & GEMM_SCHED_TAIL_SPLIT) && use_pair && load_tma && store_tma && !sk.enabled &&
+        persistent)
+        tp = plan_tail(p.num_tiles, p.num_kb, programs);
+    void *tail_ws = nullptr;
+    if (tp.splits > 1) {
+        tail_ws = symbol_address(g_tail_addr[dev], g_tail_scratch);
+        if (tail_ws == nullptr) return GEMM_ERR_CUDA;
+        // slot v: rows [256 v, 256 v + 256) of a 256-column fp32 matrix
+        if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tail_ws, pair::TILE_N,
+                       uint64_t(tp.splits) * tp.tiles * pair::TILE_M, pair::TILE_N * 4u, EPI_COLS, 32))
+            return GEMM_ERR_CUDA;
+        p.tail_first = tp.first;
+        p.tail_tiles = tp.tiles;
+        p.tail_kps = tp.kps;
+        p.num_units = tp.first + tp.splits * tp.tiles;
+    }
     const int grid_programs = int(p.num_units < programs ? p.num_units : programs);
     if (use_pair && int64_t(grid_programs) * 2 > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     const int grid = use_pair ? 2 * grid_programs : grid_programs;
     if (log_enabled())
         std::fprintf(stderr,
                      "[gemm_f16] M=%lld N=%lld K=%lld kernel=%s tiles=%d grid=%d load=%s store=%s A=%s "
-                     "B=%s order=%s G=%d cross_tile=%u persistent=%d dynamic=%u splits=%d\n",
+                     "B=%s order=%s G=%d cross_tile=%u persistent=%d dynamic=%u splits=%d tail=%dx%d\n",
                      (long long)M, (long long)N, (long long)K, use_pair ? "cta-pair 256x256" : "one-cta 128x256",
                      p.num_tiles, grid,
                      load_tma ? "tma" : "predicated", store_tma ? "tma" : "predicated",
                      p.a_mn ? "m-major" : "k-major", p.b_mn ? "n-major" : "k-major",
                      grouped ? "grouped" : "row-major", p.sched.group_m, p.cross_tile, int(persistent),
-                     p.dynamic, sp.splits);
+                     p.dynamic, sp.splits, tp.tiles, tp.splits);
 
     cudaError_t e;
     if (split) {
-        e = dynamic ? launch_pair<true, true, true>(tmA, tmB, tmC, p, cm, grid, stream)
-                    : launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
+        e = dynamic ? launch_pair<true, true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
+                    : launch_pair<true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
         if (e == cudaSuccess) {
             const int64_t quads = M * ((N + 3) / 4);
             const int threads = 256;
@@ -488,16 +578,28 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
                                                               sp.ldw, stride_cm, sp.splits, out_dtype, alpha);
             e = cudaGetLastError();
         }
+    } else if (tp.splits > 1) {
+        e = launch_pair<true, true, false, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
+        if (e == cudaSuccess) {
+            const int64_t quads = int64_t(tp.tiles) * (pair::TILE_M * pair::TILE_N / 4);
+            const int threads = 256;
+            const int64_t want = cdiv(quads, threads);
+            const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
+            tail_reduce_kernel<pair::TILE_M><<<blocks, threads, 0, stream>>>(
+                static_cast<const float *>(tail_ws), C, M, N, stride_cm, p.sched, tp.first, tp.tiles, tp.splits,
+                out_dtype, alpha);
+            e = cudaGetLastError();
+        }
     } else if (dynamic) {
-        e = store_tma ? launch_pair<true, true, true>(tmA, tmB, tmC, p, cm, grid, stream)
-                      : launch_pair<true, false, true>(tmA, tmB, tmC, p, cm, grid, stream);
+        e = store_tma ? launch_pair<true, true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
+                      : launch_pair<true, false, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
     } else if (use_pair) {
         if (load_tma)
-            e = store_tma ? launch_pair<true, true>(tmA, tmB, tmC, p, cm, grid, stream)
-                          : launch_pair<true, false>(tmA, tmB, tmC, p, cm, grid, stream);
+            e = store_tma ? launch_pair<true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
+                          : launch_pair<true, false>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
         else
-            e = store_tma ? launch_pair<false, true>(tmA, tmB, tmC, p, cm, grid, stream)
-                          : launch_pair<false, false>(tmA, tmB, tmC, p, cm, grid, stream);
+            e = store_tma ? launch_pair<false, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
+                          : launch_pair<false, false>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
     }
     else if (load_tma && store_tma) e = launch<true, true>(tmA, tmB, tmC, p, cm, grid, stream);
     else if (load_tma) e = launch<true, false>(tmA, tmB, tmC, p, cm, grid, stream);
@@ -607,7 +709,7 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
 
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
                                    int32_t *dynamic_smem, int32_t *threads) {
-    if (variant < 0 || variant > 9) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 10) return GEMM_ERR_INVALID_ARG;
     cudaFuncAttributes a;
     cudaError_t e;
     int thr, dyn;
@@ -621,7 +723,8 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *stat
         case 6: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, true>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
         case 7: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
         case 8: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
-        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        case 9: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
     }
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;
@@ -638,6 +741,17 @@ gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t 
     w.epoch = next_epoch();
     wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(w);
     return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_f16_selftest_pair_abort(const void *A, const void *B, float *C, int64_t M, int64_t N,
+                                           int64_t K, int32_t stop_after, gemm_stream_t stream) {
+    if (stop_after < 1 || K < 1) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u) return GEMM_ERR_UNSUPPORTED;
+    if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED;  // TMA loads: 16-byte row strides
+    SplitReq sk;
+    sk.stop_after = stop_after;
+    return gemm_impl(A, B, C, M, N, K, K, 1, N, 1, N, 1, 8, GEMM_SCHED_GROUPED | GEMM_SCHED_CROSS_TILE, stream,
+                     sk);
 }
 
 gemm_status_t gemm_f16_selftest_check(gemm_stream_t stream_) {
@@ -688,29 +802,9 @@ constexpr uint64_t kNoAllocScratchBytes = 32ull << 20;  // 32 MiB, held by every
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// The scratch array's device address on each device. Only a successful lookup
-// is kept: a lookup that fails (say, during a stream capture, or with an error
-// left over from earlier work) returns GEMM_ERR_CUDA and the next call retries.
-struct ScratchState {
-    std::mutex mu;
-    std::atomic<void *> ptr{nullptr};
-};
-ScratchState g_scratch[kMaxDevices];
-
-void *scratch_address(int dev) {
-    ScratchState &s = g_scratch[dev];
-    void *p = s.ptr.load(std::memory_order_acquire);
-    if (p != nullptr) return p;
-    std::lock_guard<std::mutex> lock(s.mu);
-    p = s.ptr.load(std::memory_order_relaxed);
-    if (p != nullptr) return p;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
-        (void)cudaGetLastError();
-        return nullptr;
-    }
-    s.ptr.store(p, std::memory_order_release);
-    return p;
-}
+// The scratch array's device address on each device (kept once a lookup
+// succeeds; a failed one returns GEMM_ERR_CUDA and the next call retries).
+SymbolAddress g_scratch[kMaxDevices];
 
 }  // namespace
 
@@ -732,7 +826,7 @@ extern "C" gemm_status_t gemm_f16_splitk_noalloc(const void *A, const void *B, f
         // looked up with the device current, and kept once a lookup succeeds.
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
-        ws = scratch_address(dev);
+        ws = symbol_address(g_scratch[dev], g_noalloc_scratch);
         if (ws == nullptr) return GEMM_ERR_CUDA;
     }
     return gemm_f16_splitk(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm,

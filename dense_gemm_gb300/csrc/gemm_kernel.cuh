@@ -254,7 +254,15 @@ struct Params {
     // slice s of the workspace (3-D tensor map in place of C's) instead of C.
     int32_t splits;     // >= 1
     int32_t kb_per_split;
-    int32_t num_units;  // num_tiles * splits
+    int32_t num_units;  // num_tiles * splits, or with a split tail tail_first + tail_splits * tail_tiles
+    // Split tail (CTA-pair kernel, GEMM_SCHED_TAIL_SPLIT): units below tail_first
+    // are whole tiles; the last tail_tiles tiles (fewer than one round of
+    // programs) are split along K into slices of tail_kps k-blocks. Unit
+    // tail_first + v covers tile tail_first + v % tail_tiles and slice
+    // v / tail_tiles, and stores its fp32 partial tile into slot v of the scratch.
+    int32_t tail_first;
+    int32_t tail_tiles;
+    int32_t tail_kps;
     uint32_t a_mn;      // 1: A is M-major in memory (and in shared memory)
     uint32_t b_mn;      // 1: B is N-major
     uint32_t idesc;     // tcgen05 instruction descriptor
@@ -270,6 +278,10 @@ struct Params {
     uint32_t cls_mis[2];
     uint32_t cls_live[2];
     float alpha;        // C = alpha * (A @ B)
+    // Failure-detection self-test only (0 otherwise): the CTA-pair producers
+    // issue no copies once they have issued this many stages, and keep waiting
+    // for stages to be freed, so that the MMA warp's wait runs out.
+    int32_t stop_after;
     WaitCtl wait;
 };
 
@@ -502,16 +514,11 @@ __device__ __forceinline__ void place_class_group(const Params &p, const GroupSh
 // store, which clips the M/N edges. Otherwise: transpose through the staging
 // buffer so each store instruction writes 32 consecutive floats of one row.
 // `drained()` runs on every lane right after the warp's last TMEM load.
-//
-// Pacing: every program walks the same tile sequence in step, so without it all
-// epilogues would write their C tiles in the same few microseconds, a burst that
-// saturates HBM and stalls the next tile's operand loads. For long work units
-// the chunks are spread over the next unit's main loop (the accumulator is only
-// needed again two units later). Measured at 16384^2 x 4096: tensor-pipe
-// activity 89 % -> 92 %.
-// Without cross-tile overlap the producer waits for the epilogue, and after a
-// program's last unit no main loop follows: then there is nothing to spread
-// the stores over.
+// The chunks are stored as fast as they come: spacing them out over the next
+// unit's main loop by a fixed sleep per k-block measured the same (device-timed
+// on GB300, 16384^2 x K for K = 512 ... 4096 and 8192^2 x 4096, within 0.7 %
+// both in short loops and under the power limit), so nothing here depends on
+// the clock.
 constexpr int EPI_CHUNKS32 = BN / EPI_COLS;  // 8 fp32 chunks of 32 columns per accumulator row block
 constexpr int EPI_CHUNKS16 = BN / 64;        // 4 chunks of 64 16-bit values
 // Work units shorter than this many K-blocks split each row block's chunks
@@ -536,19 +543,21 @@ __device__ __forceinline__ void epilogue_chunks(int32_t unit_kblocks, bool last_
     }
 }
 
-__device__ __forceinline__ uint32_t epilogue_pace_ns(int32_t unit_kblocks, uint32_t cross_tile,
-                                                     int chunks_per_warp, bool last_unit) {
-    // about 160 ns per K-block of spread over a warp's chunks
-    return (cross_tile && !last_unit && unit_kblocks >= 32 && chunks_per_warp > 0)
-               ? uint32_t(unit_kblocks) * 160u / uint32_t(chunks_per_warp)
-               : 0u;
-}
+// Where a partial tile of a split tail unit goes: the scratch map, the row of
+// the scratch that holds this warp's first tile row, and the tile's first
+// column of C (scratch columns are tile-local).
+struct TailStore {
+    const CUtensorMap *map;
+    int32_t row;
+    int64_t col_base;
+};
 
 // Stores one 32 x 32 fp32 chunk (this lane's row, 32 columns from col0).
 template <bool kTmaStore>
 __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, int64_t col0, const Params &p,
-                                              const CUtensorMap *tmC, uint32_t stg, int lane, int32_t split) {
-    if (p.alpha != 1.0f) {
+                                              const CUtensorMap *tmC, uint32_t stg, int lane, int32_t split,
+                                              const TailStore *ts = nullptr) {
+    if (p.alpha != 1.0f && ts == nullptr) {  // a split tail's partials are scaled once summed
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(p.alpha * __uint_as_float(v[i]));
     }
@@ -561,7 +570,10 @@ __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, i
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (row0 < p.M && col0 < p.N) {
+            if (ts != nullptr) {  // split tail: partial tile -> its scratch slot (always in bounds)
+                if (row0 < p.M && col0 < p.N)
+                    tma_store_2d_hint(ts->map, stg, int32_t(col0 - ts->col_base), ts->row, l2_policy_evict_normal());
+            } else if (row0 < p.M && col0 < p.N) {
                 if (p.splits > 1)  // partial tile -> workspace slice `split`, read once by the reduction
                     tma_store_3d_hint(tmC, stg, int32_t(col0), int32_t(row0), split, l2_policy_evict_normal());
                 else if (p.l2_mode & 1u)  // C is never read again: do not keep it in L2
@@ -594,7 +606,8 @@ __device__ __forceinline__ void store_chunk32(uint32_t (&v)[32], int64_t row0, i
 template <bool kTmaStore, typename Drained>
 __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int64_t col_base, int c0, int n,
                                               const Params &p, const CUtensorMap *tmC, uint32_t stg, int lane,
-                                              Drained drained, int32_t split = 0, uint32_t pace_ns = 0) {
+                                              Drained drained, int32_t split = 0,
+                                              const TailStore *ts = nullptr) {
     if (n == 0) {
         drained();
         return;
@@ -605,16 +618,14 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
     for (int c = c0; c < c0 + n; c += 2) {
         tmem_ld_wait();
         tmem_ld_32x32b_x32(t_row + (c + 1) * EPI_COLS, vb);
-        store_chunk32<kTmaStore>(va, row0, col_base + c * EPI_COLS, p, tmC, stg, lane, split);
-        if (pace_ns != 0) __nanosleep(pace_ns);
+        store_chunk32<kTmaStore>(va, row0, col_base + c * EPI_COLS, p, tmC, stg, lane, split, ts);
         tmem_ld_wait();
         const bool more = c + 2 < c0 + n;
         if (more)
             tmem_ld_32x32b_x32(t_row + (c + 2) * EPI_COLS, va);
         else
             drained();
-        store_chunk32<kTmaStore>(vb, row0, col_base + (c + 1) * EPI_COLS, p, tmC, stg, lane, split);
-        if (pace_ns != 0 && more) __nanosleep(pace_ns);
+        store_chunk32<kTmaStore>(vb, row0, col_base + (c + 1) * EPI_COLS, p, tmC, stg, lane, split, ts);
     }
 }
 
@@ -682,7 +693,7 @@ __device__ __forceinline__ void store_chunk16(uint32_t (&w)[32], int64_t row0, i
 template <bool kTmaStore, typename Drained>
 __device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, int64_t col_base, int c0, int n,
                                                 const Params &p, const CUtensorMap *tmC, uint32_t stg,
-                                                int lane, Drained drained, uint32_t pace_ns = 0) {
+                                                int lane, Drained drained) {
     if (n == 0) {
         drained();
         return;
@@ -703,8 +714,21 @@ __device__ __forceinline__ void epilogue_tile16(uint32_t t_row, int64_t row0, in
             drained();
         pack_half_chunk(vb, w + 16, alpha, p.out_dtype);
         store_chunk16<kTmaStore>(w, row0, col_base + c * 64, p, tmC, stg, lane);
-        if (pace_ns != 0 && more) __nanosleep(pace_ns);
     }
+}
+
+// A unit of the split tail (u >= tail_first): its tile, k-block range and
+// scratch slot; other units keep what the caller decoded, with slot -1.
+__device__ __forceinline__ void tail_unit(const Params &p, int32_t u, int32_t &tile, int32_t &kb0,
+                                          int32_t &kb1, int32_t &slot) {
+    slot = -1;
+    if (u < p.tail_first) return;
+    const int32_t v = u - p.tail_first;
+    const int32_t j = v / p.tail_tiles;
+    tile = p.tail_first + (v - j * p.tail_tiles);
+    kb0 = j * p.tail_kps;
+    kb1 = min(p.num_kb, kb0 + p.tail_kps);
+    slot = v;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -945,12 +969,10 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
             int c0, n;
             if (p.out_dtype == 0) {
                 epilogue_chunks(num_kb, last, half, EPI_CHUNKS32, c0, n);
-                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, 0,
-                                         epilogue_pace_ns(num_kb, p.cross_tile, n, last));
+                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release);
             } else {
                 epilogue_chunks(num_kb, last, half, EPI_CHUNKS16, c0, n);
-                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
-                                           epilogue_pace_ns(num_kb, p.cross_tile, n, last));
+                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release);
             }
         }
         if (kTmaStore && lane == 0) bulk_wait_group<0>();
@@ -1047,6 +1069,67 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ W, void *__restri
             if (j + 1 < N) c[1] = acc.y;
             if (j + 2 < N) c[2] = acc.z;
             if (j + 3 < N) c[3] = acc.w;
+        }
+    }
+}
+
+// Split tail: C over each tail tile = the sum, in slice order 0, 1, ..., S-1,
+// of its S fp32 partial tiles in the scratch (slot j * tail_tiles + i holds
+// slice j of tail tile i; TILE x TILE floats each, row-major), times alpha,
+// rounded to C's type. Fixed order: the result does not depend on scheduling.
+// Four consecutive columns per thread.
+template <int TILE>
+__global__ void tail_reduce_kernel(const float *__restrict__ W, void *__restrict__ Cv, int64_t M, int64_t N,
+                                   int64_t scm, Sched sched, int32_t first, int32_t tiles, int32_t S,
+                                   uint32_t out_dtype, float alpha) {
+    constexpr int QUADS = TILE * TILE / 4;
+    const int64_t total = int64_t(tiles) * QUADS;
+    float *C = static_cast<float *>(Cv);
+    const bool vec_c = (scm % 4 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0);
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int32_t i = int32_t(e / QUADS);
+        const int32_t q = int32_t(e - int64_t(i) * QUADS);
+        const int32_t r = q / (TILE / 4), c = (q - r * (TILE / 4)) * 4;
+        int32_t tm, tn;
+        tile_coords(first + i, sched, tm, tn);
+        const int64_t row = int64_t(tm) * TILE + r, col = int64_t(tn) * TILE + c;
+        if (row >= M || col >= N) continue;
+        const float *w = W + (int64_t(i) * TILE + r) * TILE + c;
+        const int64_t slot = int64_t(tiles) * TILE * TILE;
+        float4 acc = *reinterpret_cast<const float4 *>(w);
+        for (int32_t s = 1; s < S; ++s) {
+            const float4 v = *reinterpret_cast<const float4 *>(w + s * slot);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (alpha != 1.0f) {
+            acc.x *= alpha;
+            acc.y *= alpha;
+            acc.z *= alpha;
+            acc.w *= alpha;
+        }
+        if (!G16_CHECK(row >= 0 && col >= 0)) continue;
+        if (out_dtype != 0) {
+            uint16_t *c16 = static_cast<uint16_t *>(Cv) + row * scm + col;
+            const uint32_t w01 = pack_16x2(acc.x, acc.y, out_dtype);
+            const uint32_t w23 = pack_16x2(acc.z, acc.w, out_dtype);
+            c16[0] = uint16_t(w01 & 0xffffu);
+            if (col + 1 < N) c16[1] = uint16_t(w01 >> 16);
+            if (col + 2 < N) c16[2] = uint16_t(w23 & 0xffffu);
+            if (col + 3 < N) c16[3] = uint16_t(w23 >> 16);
+            continue;
+        }
+        float *cp = C + row * scm + col;
+        if (vec_c && col + 3 < N) {
+            *reinterpret_cast<float4 *>(cp) = acc;
+        } else {
+            cp[0] = acc.x;
+            if (col + 1 < N) cp[1] = acc.y;
+            if (col + 2 < N) cp[2] = acc.z;
+            if (col + 3 < N) cp[3] = acc.w;
         }
     }
 }

@@ -95,11 +95,16 @@ constexpr int THREADS = Layout<true>::threads;
 
 // kDyn: units handed out by cluster launch control (TMA loads only); a
 // separate instantiation, so the static schedule carries none of its code.
-template <bool kTmaLoad, bool kTmaStore, bool kDyn = false>
+// kTail (TMA loads and stores, static schedule): the tiles of a last, partial
+// round are split along K across the programs that round would leave idle;
+// their fp32 partial tiles go to the scratch described by tmW, and a second
+// kernel sums them into C.
+template <bool kTmaLoad, bool kTmaStore, bool kDyn = false, bool kTail = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoad>::threads, 1)
     gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmC, const Params p,
-                  const __grid_constant__ typename ClassMapsFor<kTmaLoad>::type cm) {
+                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                  const Params p, const __grid_constant__ typename ClassMapsFor<kTmaLoad>::type cm) {
+    static_assert(!kTail || (kTmaLoad && kTmaStore && !kDyn), "split tail: TMA loads and stores, static stream");
     using Lay = pair::Layout<kTmaLoad>;
     constexpr int NST = Lay::stages;
     constexpr int LOAD_WARPS = Lay::load_warps;
@@ -321,9 +326,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             };
             if (dyn && rank == 0) request();
             for (int32_t u = pair_id; ok && (!kDyn || u >= 0) && u < p.num_units; ++it) {
-                const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
-                const int32_t kb0 = split * p.kb_per_split;
-                const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+                int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
+                int32_t kb0 = split * p.kb_per_split;
+                int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+                if constexpr (kTail) {
+                    int32_t slot;
+                    tail_unit(p, u, tile, kb0, kb1, slot);
+                }
                 int32_t tm, tn;
                 tile_coords(tile, p.sched, tm, tn);
                 if (!p.cross_tile && it > 0) {
@@ -334,6 +343,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 const int32_t n0 = tn * pair::TILE_N + int32_t(rank) * pair::CTA_N;
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
+                    if (p.stop_after > 0 && issued >= uint32_t(p.stop_after)) {  // self-test: nothing more
+                        if (++stage == NST) { stage = 0; phase ^= 1u; }
+                        continue;
+                    }
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair::PAIR_TX_BYTES);
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     const int32_t k0 = kb * BK;
@@ -453,8 +466,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             const DescStep db = make_desc_step(sB, p.b_mn, pair::B_STAGE_BYTES);
             const uint32_t idesc = p.idesc;
             for (int32_t u = pair_id; ok && (!kDyn || u >= 0) && u < p.num_units; ++it) {
-                const int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
-                const int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+                int32_t kb0 = (u / p.num_tiles) * p.kb_per_split;
+                int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+                if constexpr (kTail) {
+                    int32_t tile = 0, slot;
+                    tail_unit(p, u, tile, kb0, kb1, slot);
+                }
                 const uint32_t acc = it & 1, use = it >> 1;
                 // both CTAs' epilogues have released this accumulator (remote arrivals)
                 if (!__all_sync(0xffffffffu,
@@ -505,9 +522,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         const uint32_t stg = base + Lay::off_epi + uint32_t(ew) * (EPI_BUFS * EPI_BUF_BYTES);
         int32_t it = 0;
         for (int32_t u = pair_id; (!kDyn || u >= 0) && u < p.num_units; ++it) {
-            const int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
-            const int32_t kb0 = split * p.kb_per_split;
-            const int32_t unit_kb = min(num_kb, kb0 + p.kb_per_split) - kb0;
+            int32_t tile = u % p.num_tiles, split = u / p.num_tiles;
+            int32_t kb0 = split * p.kb_per_split;
+            int32_t kb1 = min(num_kb, kb0 + p.kb_per_split);
+            int32_t slot = -1;
+            if constexpr (kTail) tail_unit(p, u, tile, kb0, kb1, slot);
+            const int32_t unit_kb = kb1 - kb0;
             int32_t tm, tn;
             tile_coords(tile, p.sched, tm, tn);
             const uint32_t acc = it & 1, use = it >> 1;
@@ -532,14 +552,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             else
                 last = u + num_pairs >= p.num_units;
             int c0, n;
-            if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
+            if (kTail && slot >= 0) {  // partial tile of the split tail -> scratch slot, fp32
+                const TailStore ts{&tmW, int32_t(slot * pair::TILE_M + int32_t(rank) * pair::CTA_M + q * 32),
+                                   col_base};
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
-                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split,
-                                         epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
+                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, 0, &ts);
+            } else if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
+                epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
+                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split);
             } else {
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS16, c0, n);
-                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release,
-                                           epilogue_pace_ns(unit_kb, p.cross_tile, n, last));
+                epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release);
             }
             if constexpr (kDyn) {
                 if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) break;

@@ -70,7 +70,12 @@ typedef enum {
                                      cluster per tile and let resident clusters take the
                                      tiles of clusters that have not started (cluster launch
                                      control), in ascending tile_id; ignored otherwise */
-#define GEMM_SCHED_ALL_FLAGS 0x1Fu
+#define GEMM_SCHED_TAIL_SPLIT 0x20u /* CTA-pair tiles, TMA-loadable A and B, TMA-storable C,
+                                       persistent static order: when the last round of
+                                       tiles would leave at least three quarters of the
+                                       programs idle, split those tiles along K across the
+                                       idle programs (see gemm_f16) */
+#define GEMM_SCHED_ALL_FLAGS 0x3Fu
 
 /*
  * gemm_f16 — C = A @ B.
@@ -105,6 +110,19 @@ typedef enum {
  * GEMM_SCHED_SINGLE_CTA into 128x256 tiles of one CTA each. The tile order
  * (row-major / grouped) applies to whichever tiles are used; a "program" of
  * the persistent order is a CTA pair or a CTA.
+ * GEMM_SCHED_TAIL_SPLIT (the pages only name Stream-K, [persistent] "naive
+ * persistent matmul"): the tiles of the last round, t of them with t <= P/4,
+ * become S >= 2 units each (consecutive K slices of at least 8 k-blocks of 64;
+ * S*t <= P), computed by the programs that round would leave idle: unit
+ * T - t + v is slice v / t of tile
+ * T - t + v % t. Their fp32 partial tiles go to a 24 MiB scratch array built
+ * into the library (held by every GPU that loads it); a second kernel on the
+ * same stream sums each tile's slices in slice order 0, 1, ..., scales by alpha
+ * and rounds into C. Results are deterministic, but the tail tiles' sums are no
+ * longer bit-identical to the unsplit order's; integer-valued inputs (every
+ * partial sum exact) stay exact. Calls with this flag that overlap on the GPU
+ * share the scratch and race: serialise them. Where the conditions above do
+ * not hold the flag has no effect.
  * GEMM_SCHED_NON_PERSISTENT launches one program per tile ([persistent]
  * "naive tiled matmul" grid); program p then computes tile_id p only, and
  * GEMM_SCHED_CROSS_TILE has nothing to overlap. GEMM_SCHED_DYNAMIC (no
@@ -263,7 +281,8 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags,
  * 1 = TMA loads + predicated store, 2 = predicated loads + TMA store,
  * 3 = predicated loads + predicated store. CTA-pair tiles, in the same
  * order: 4, 5, 6, 7; with GEMM_SCHED_DYNAMIC (TMA loads): 8 = TMA store,
- * 9 = predicated store. Outputs may be NULL. Needs a device.
+ * 9 = predicated store; 10 = the CTA-pair kernel with a split tail
+ * (GEMM_SCHED_TAIL_SPLIT). Outputs may be NULL. Needs a device.
  */
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *static_smem, int32_t *dynamic_smem,
@@ -300,6 +319,25 @@ gemm_status_t gemm_f16_set_wait_timeout(uint64_t ns);
  * gemm_f16_sync_status) and the kernel returns; the CUDA context stays usable.
  */
 gemm_status_t gemm_f16_selftest_wait_timeout(uint64_t timeout_ns, gemm_stream_t stream);
+
+/*
+ * gemm_f16_selftest_pair_abort — failure-detection self-test of the CTA-pair
+ * kernel (no counterpart on the pages). Enqueues gemm_f16 on row-major A
+ * [M,K], B [K,N] and C [M,N] (device, 16-byte-aligned A and B, K and N
+ * multiples of 8; otherwise GEMM_ERR_UNSUPPORTED), grouped order with
+ * GEMM_SCHED_CROSS_TILE, except that both CTAs of every pair stop issuing
+ * copies once they have issued `stop_after` (>= 1) pipeline stages, while
+ * still waiting for stages to be freed as in a normal run. No stage is then
+ * left half-counted, and the MMA warp's wait for the first missing stage runs
+ * out after the current wait limit (gemm_f16_set_wait_timeout): the kernel
+ * records GEMM_ERR_TIMEOUT, every CTA's other waits give up, each CTA waits
+ * (bounded) for its own work in flight, frees its TMEM and returns. The
+ * sticky status is read and cleared by gemm_f16_sync_status; C is undefined
+ * and the context stays usable.
+ */
+gemm_status_t gemm_f16_selftest_pair_abort(const void *A, const void *B, float *C,
+                                           int64_t M, int64_t N, int64_t K, int32_t stop_after,
+                                           gemm_stream_t stream);
 
 /*
  * gemm_f16_selftest_check — debug build (GEMM_DEBUG) only: launches one

@@ -43,7 +43,7 @@ def assert_within_bound(got: np.ndarray, ref: np.ndarray, A, B, what=""):
 
 
 def run(A_host, B_host, grouped=True, cross_tile=True, G=8, out_layout=None, single_cta=False,
-        persistent=True, dynamic=False):
+        persistent=True, dynamic=False, tail_split=False):
     """C = A @ B through the C ABI; returns (C_device_fp32, C_host_numpy)."""
     A = to_dev(A_host)
     B = to_dev(B_host)
@@ -54,7 +54,7 @@ def run(A_host, B_host, grouped=True, cross_tile=True, G=8, out_layout=None, sin
         buf = torch.full((off + M * ld,), float("nan"), dtype=torch.float32, device="cuda")
         out = buf.as_strided((M, N), (ld, 1), off)
     C = gemm(A, B, out, group_size_m=G, grouped=grouped, cross_tile=cross_tile,
-             single_cta=single_cta, persistent=persistent, dynamic=dynamic)
+             single_cta=single_cta, persistent=persistent, dynamic=dynamic, tail_split=tail_split)
     torch.cuda.synchronize()
     return C, C.cpu().numpy().astype(np.float64)
 

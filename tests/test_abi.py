@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert "gemm_f16" in names and "gemm_f16_tile_map" in names
-    assert len(names) == 13, names
+    assert len(names) == 14, names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -56,7 +56,7 @@ def _call(lib, **kw):
 
 @pytest.mark.parametrize("kw", [dict(M=-1), dict(N=-5), dict(K=-1), dict(M=2 ** 31),
                                 dict(sam=0), dict(sak=-1), dict(sbk=0), dict(sbn=0), dict(scm=0),
-                                dict(scn=0), dict(G=0), dict(G=-3), dict(flags=32),
+                                dict(scn=0), dict(G=0), dict(G=-3), dict(flags=64),
                                 dict(flags=0x80000000), dict(C=0), dict(A=0), dict(B=0),
                                 dict(scm=3)])
 def test_invalid_arguments(lib, kw):
@@ -96,7 +96,7 @@ def test_config_without_device(lib):
     cfg = get_config(0, 0, single_cta=True)
     assert (cfg["bm"], cfg["bn"], cfg["bk"]) == (128, 256, 64)
     assert lib.gemm_f16_get_config(-1, 4, 0, None, None, None, None, None) == 1
-    assert lib.gemm_f16_get_config(4, 4, 32, None, None, None, None, None) == 1
+    assert lib.gemm_f16_get_config(4, 4, 64, None, None, None, None, None) == 1
 
 
 def test_wait_timeout_validation(lib):
@@ -112,7 +112,7 @@ def test_product_library_has_no_device_checks(lib):
 
 def test_kernel_info_rejects_unknown_variant(lib):
     i32 = ctypes.POINTER(ctypes.c_int32)
-    assert lib.gemm_f16_kernel_info(10, i32(), i32(), i32(), i32()) == 1
+    assert lib.gemm_f16_kernel_info(11, i32(), i32(), i32(), i32()) == 1
     assert lib.gemm_f16_kernel_info(-1, i32(), i32(), i32(), i32()) == 1
 
 

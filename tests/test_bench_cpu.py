@@ -48,7 +48,7 @@ def test_kernel_source_hash_covers_the_kernel_sources():
 
 
 @pytest.mark.parametrize("sweep", ["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
-                                   "outdtype", "ragged", "schedule"])
+                                   "outdtype", "ragged", "schedule", "tail"])
 def test_sweeps_parse(sweep):
     a = bench.parse_args(["--sweep", sweep, "--steps", "3", "--warmup", "3"])
     assert a.sweep == sweep and a.steps == 3 and a.warmup == 3

@@ -264,8 +264,8 @@ def test_invalid_arguments_raise():
 
 def test_kernel_resources():
     # warps: producer (1; predicated loads: 3 for one CTA, 4 + 1 issuer per CTA of a pair) + MMA + 8 epilogue
-    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448, 8: 320, 9: 320}
-    for v in range(10):
+    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448, 8: 320, 9: 320, 10: 320}
+    for v in range(11):
         info = kernel_info(v)
         assert info["dynamic_smem"] <= 232448 and info["regs_per_thread"] <= 255
         assert info["threads_per_cta"] == threads[v]
@@ -408,7 +408,7 @@ def test_full_16384x16384x4096_single_cta():
     _full("square_16384x16384x4096", grouped=True, cross=True, count=16, single=True)
 
 
-@pytest.mark.parametrize("K", [128, 512, 1024, 2048])
+@pytest.mark.parametrize("K", [128, 512, 1024, 2048, 4096])
 @pytest.mark.parametrize("cross", [True, False])
 def test_full_k_sweep(K, cross):
     _full(f"ksweep_16384x16384x{K}", grouped=True, cross=cross, count=32)
@@ -438,6 +438,31 @@ def test_bounded_wait_times_out_and_context_survives():
     A = draw(300, 200, "int", 99)
     B = draw(200, 400, "int", 98)
     assert np.array_equal(run(A, B)[1], oracle.gemm(A, B))
+
+
+# stages per pair: 16 (one tile each); 20 for the pairs with two tiles, 10 for the others
+# (those finish normally while the rest abort in their second tile); 4
+@pytest.mark.parametrize("M,N,K,stop_after", [(512, 512, 1024, 3), (2304, 2560, 640, 15), (300, 520, 256, 2)])
+def test_pair_kernel_abort_returns_and_context_survives(M, N, K, stop_after):
+    """Both CTAs of every pair stop issuing copies after `stop_after` stages:
+    the MMA warp's wait runs out, the launch records GEMM_ERR_TIMEOUT and every
+    CTA (the second of each pair included) returns; the next GEMM is exact."""
+    from dense_gemm_gb300 import selftest_pair_abort, set_wait_timeout
+    assert sync_status() == 0
+    A = to_dev(draw(M, K, "int", 700))
+    B = to_dev(draw(K, N, "int", 701))
+    C = torch.empty(M, N, device="cuda")
+    set_wait_timeout(5_000_000)  # 5 ms
+    try:
+        selftest_pair_abort(A, B, C, stop_after)
+        assert sync_status() == 4  # GEMM_ERR_TIMEOUT, read and cleared
+        assert sync_status() == 0
+    finally:
+        set_wait_timeout(2_000_000_000)
+    Ah = draw(700, 300, "int", 702)
+    Bh = draw(300, 900, "int", 703)
+    assert np.array_equal(run(Ah, Bh)[1], oracle.gemm(Ah, Bh))
+    assert sync_status() == 0
 
 
 # ------------------------------------------------------------------ host-operand APIs
@@ -516,6 +541,100 @@ def test_splitk_rejects_small_workspace_and_unaligned_operands():
     with pytest.raises(GemmError) as e:
         gemm_splitk(A2, B2, splits=2)
     assert e.value.status == 2
+
+
+# ------------------------------------------------------------------ split tail (GEMM_SCHED_TAIL_SPLIT)
+
+def _tail_plan(M, N, K):
+    """(first, tiles, slices) the library plans for the split tail, restated from
+    the header's rule with the current device's pair count."""
+    cfg = get_config(M, N)
+    T = -(-M // cfg["bm"]) * -(-N // cfg["bn"])
+    P = get_config(16384, 16384)["grid"]
+    nkb = -(-K // cfg["bk"])
+    rest = T % P
+    if rest == 0 or 4 * rest > P:
+        return None
+    S = min(P // rest, 96 // rest, nkb // 8)
+    if S < 2:
+        return None
+    kps = -(-nkb // S)
+    S = -(-nkb // kps)
+    return (T - rest, rest, S) if S >= 2 else None
+
+
+@pytest.mark.parametrize("shape", [(512, 512, 1024), (700, 1200, 1100), (2304, 2560, 1280), (4000, 5000, 1200),
+                                   (300, 304, 4096), (2176, 384, 1000)])
+@pytest.mark.parametrize("grouped,cross", [(True, True), (False, True), (True, False)])
+def test_tail_split_integer_bit_exact(shape, grouped, cross):
+    """The split tail's slices of a tile are summed in a fixed order; with
+    integer inputs every partial sum is exact, so C equals the oracle."""
+    M, N, K = shape
+    assert _tail_plan(M, N, K) is not None  # these shapes do split their tail
+    A = draw(M, K, "int", 600 + M)
+    B = draw(K, N, "int", 601 + N)
+    ref = oracle.gemm(A, B)
+    for _ in range(2):  # the second call reuses the scratch
+        _, C = run(A, B, grouped=grouped, cross_tile=cross, G=3, tail_split=True)
+        assert np.array_equal(C, ref)
+
+
+@pytest.mark.parametrize("dtype,name", OUT_TYPES)
+@pytest.mark.parametrize("alpha", [1.0, 0.5, -2.0])
+def test_tail_split_out_dtype_alpha_bit_exact(dtype, name, alpha):
+    M, N, K = 2304, 2560, 1280
+    A = draw(M, K, "int", 610)
+    B = relayout(draw(K, N, "int", 611), "col")
+    want = oracle.round_output(oracle.gemm(A, B), name, alpha)
+    C = gemm(to_dev(A), to_dev(B), out_dtype=dtype, alpha=alpha, tail_split=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.double().cpu().numpy(), want)
+
+
+def test_tail_split_random_within_bound_and_unsplit_tiles_identical():
+    """Random operands: within the stated bound; the tiles outside the tail are
+    computed exactly as without the flag (same bits), the tail tiles differ at
+    most by the bound."""
+    M, N, K = 2304, 2560, 4096
+    A = draw(M, K, "normal", 620)
+    B = draw(K, N, "normal", 621)
+    ref = oracle.gemm(A, B)
+    _, C0 = run(A, B)
+    _, C1 = run(A, B, tail_split=True)
+    assert_within_bound(C1, ref, A, B, "tail split")
+    first, tiles, S = _tail_plan(M, N, K)
+    cfg = get_config(M, N)
+    nm, nn = -(-M // cfg["bm"]), -(-N // cfg["bn"])
+    sched = oracle.schedule(nm, nn, 8, True, 1)
+    tail = np.zeros((M, N), bool)
+    for t in range(first, first + tiles):
+        tm, tn = int(sched[t, 1]), int(sched[t, 2])
+        tail[tm * cfg["bm"]:(tm + 1) * cfg["bm"], tn * cfg["bn"]:(tn + 1) * cfg["bn"]] = True
+    assert np.array_equal(C1[~tail], C0[~tail])
+
+
+def test_tail_split_without_effect_where_it_does_not_apply():
+    """No partial last round, predicated operands, a predicated C store, one-CTA
+    tiles: the flag changes nothing (bit-identical)."""
+    P = get_config(16384, 16384)["grid"]
+    cases = [((256, 256 * (P - 1), 256), {}),  # P - 1 tiles: the last round is nearly full
+             ((512, 512, 512), {}),  # 8 k-blocks: too short to split
+             ((300, 300, 257), {}), ((512, 509, 1024), {}), ((1000, 1200, 1100), {"single_cta": True})]
+    for (M, N, K), kw in cases:
+        A = draw(M, K, "normal", 630 + M)
+        B = draw(K, N, "normal", 631 + N)
+        _, C0 = run(A, B, **kw)
+        _, C1 = run(A, B, tail_split=True, **kw)
+        assert np.array_equal(C0, C1), (M, N, K, kw)
+
+
+def test_full_ragged_4000x5000x3000_tail_split():
+    w = WORKLOADS["ragged_4000x5000x3000"]
+    A, B = w.operands()
+    _, C = run(A, B, tail_split=True)
+    check_sampled_tiles(C, A, B, count=64, seed=w.seed, what="4000x5000x3000 tail split")
+    check_sampled_rows(C, A, B, count=4000, seed=w.seed, what="4000x5000x3000 tail split")
+    check_row_col_sums(C, A, B, what="4000x5000x3000 tail split")
 
 
 # ------------------------------------------------------------------ 16-bit C and alpha
