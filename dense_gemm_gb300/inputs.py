@@ -99,6 +99,11 @@ WORKLOADS = {
                                       b_layout="col", seed=1050, tags=("ragged",)),
     "ragged_8191x8191x257": Workload("ragged_8191x8191x257", 8191, 8191, 257, "uniform",
                                      b_layout="col", seed=1060, tags=("ragged",)),
+    # the headline's B operand (16384 columns: one grouped band of B panels larger
+    # than L2) with half its rows: the case for multi-pass profiler captures of the
+    # headline's L2 behaviour (not one of the pages' shapes)
+    "half_8192x16384x4096": Workload("half_8192x16384x4096", 8192, 16384, 4096, "normal", seed=1080,
+                                     tags=("study",)),
     # few output tiles, long K: the case split-K is for (not one of the pages' shapes)
     "longk_1024x1024x32768": Workload("longk_1024x1024x32768", 1024, 1024, 32768, "uniform",
                                       seed=1070, tags=("study",)),
