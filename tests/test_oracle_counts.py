@@ -102,6 +102,56 @@ def test_padded_reads_equal_exact_when_divisible():
     assert C.reads_tiled_padded(513, 1024, 64, 128, 256) > C.reads_tiled(513, 1024, 64, 128, 256)
 
 
+def _enumerate_tile_loads(M, N, K, BM, BN, BK):
+    """Walk the tiled loop nest of "4주차 정리: Roofline과 Tiling" section 5 ("일반
+    공식") on a ragged grid: every output tile, every K step, one BM x BK piece of
+    A and one BK x BN piece of B, a piece cut by an edge still moved whole (the
+    zero-filled box of a TMA load). Returns (moved, useful) element counts, the
+    useful ones being the in-bounds elements of each piece."""
+    moved = useful = 0
+    for m0 in range(0, M, BM):
+        for n0 in range(0, N, BN):
+            for k0 in range(0, K, BK):
+                moved += BM * BK + BK * BN
+                rows, cols, ks = min(BM, M - m0), min(BN, N - n0), min(BK, K - k0)
+                useful += rows * ks + ks * cols
+    return moved, useful
+
+
+@pytest.mark.parametrize("M,N,K,BM,BN,BK", [(300, 520, 192, 128, 256, 64), (257, 513, 64, 128, 256, 64),
+                                           (1000, 90, 320, 64, 32, 32), (8, 8, 8, 4, 4, 4), (5, 7, 3, 2, 2, 1)])
+def test_padded_reads_match_an_enumeration_of_tile_loads(M, N, K, BM, BN, BK):
+    """reads_tiled_padded counts whole tiles on the cdiv grid. The enumeration
+    moves whole pieces along K too, so it equals the formula when BK divides K
+    (every case here) and exceeds the useful reads exactly on ragged grids."""
+    assert K % BK == 0
+    moved, useful = _enumerate_tile_loads(M, N, K, BM, BN, BK)
+    assert C.reads_tiled_padded(M, N, K, BM, BN) == moved
+    nm, nn = C.cdiv(M, BM), C.cdiv(N, BN)
+    # useful reads: each tile row re-reads its A rows once per tile column, and vice versa
+    assert useful == nn * M * K + nm * K * N
+    assert (moved == useful) == (M % BM == 0 and N % BN == 0)
+
+
+def test_compulsory_bytes_is_the_single_tile_limit_and_a_brute_force_count():
+    """Each input element read once and C written once: the page's tile traffic
+    HBM bytes = in * MNK(1/BM + 1/BN) + out * MN with one tile covering all of C
+    (BM = M, BN = N), and the number of distinct A, B and C elements a direct
+    triple loop touches."""
+    for M, N, K in [(512, 512, 512), (16384, 16384, 4096), (8191, 8191, 257), (4000, 5000, 3000)]:
+        assert C.compulsory_bytes(M, N, K) == C.tile_traffic_bytes(M, N, K, M, N, in_bytes=2, out_bytes=4)
+    for M, N, K in [(3, 4, 5), (6, 2, 7), (1, 1, 1)]:
+        a, b, c = set(), set(), set()
+        for i in range(M):
+            for j in range(N):
+                for k in range(K):
+                    a.add((i, k))
+                    b.add((k, j))
+                c.add((i, j))
+        assert C.compulsory_bytes(M, N, K) == 2 * len(a) + 2 * len(b) + 4 * len(c)
+        assert C.compulsory_bytes(M, N, K, in_bytes=4, out_bytes=4) == 4 * (len(a) + len(b) + len(c))
+
+
 def test_onchip_table(golden):
     g = golden("onchip_memory.json")
     e = g["elem_bytes"]
