@@ -66,6 +66,10 @@ def parse_args(argv=None):
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--single-cta", action="store_true",
                    help="one-CTA 128x256 tiles instead of CTA-pair 256x256 tiles")
+    p.add_argument("--sweep-reps", type=int, default=3,
+                   help="repetitions of each study point (interleaved); the median is reported")
+    p.add_argument("--sweep-rest", type=float, default=1.0,
+                   help="seconds of rest before each timed study point")
     p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
                                        "outdtype", "ragged", "schedule", "tail"],
                    default=None,
@@ -611,42 +615,53 @@ def run_sweep(args):
         A_host, B_host = w.operands()
         A, B = A_host.to(dev), B_host.to(dev)
         C = torch.empty((w.M, w.N), dtype=torch.float32, device=dev)
+        runs = []
         for pt in points:
-            if isinstance(pt, tuple) and pt[0] == "out16_tail":
+            if isinstance(pt, tuple) and pt[0] in ("out", "out16_tail"):
                 Cx = torch.empty((w.M, w.N), dtype=pt[1], device=dev)
-                run = lambda: gemm(A, B, Cx, group_size_m=args.group_size, tail_split=True)  # noqa: E731
-                desc = {"impl": "gemm_f16_out", "c_dtype": str(pt[1]).replace("torch.", ""), "tail_split": True}
-            elif isinstance(pt, tuple) and pt[0] == "out":
-                Cx = torch.empty((w.M, w.N), dtype=pt[1], device=dev)
-                run = lambda: gemm(A, B, Cx, group_size_m=args.group_size)  # noqa: E731
+                tail = pt[0] == "out16_tail"
+                run = (lambda Cx=Cx, tail=tail:
+                       gemm(A, B, Cx, group_size_m=args.group_size, tail_split=tail))
                 desc = {"impl": "gemm_f16_out" if pt[1] != torch.float32 else "gemm_f16",
                         "c_dtype": str(pt[1]).replace("torch.", "")}
+                if tail:
+                    desc["tail_split"] = True
             elif pt == "torch.matmul":
                 run = lambda: torch.matmul(A, B)  # noqa: E731  (cuBLAS, fp16 output)
                 desc = {"impl": "torch.matmul (cuBLAS), fp16 output"}
             elif pt == "splitk":
                 need, used = splitk_workspace_size(w.M, w.N, w.K, 0)
                 ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
-                run = lambda: gemm_splitk(A, B, C, splits=0, workspace=ws,  # noqa: E731
-                                          group_size_m=args.group_size)
+                run = (lambda ws=ws:
+                       gemm_splitk(A, B, C, splits=0, workspace=ws, group_size_m=args.group_size))
                 desc = {"impl": "gemm_f16_splitk", "splits": used, "workspace_bytes": need}
             else:
-                run = lambda: gemm(A, B, C, group_size_m=args.group_size, **pt)  # noqa: E731
+                run = lambda pt=pt: gemm(A, B, C, group_size_m=args.group_size, **pt)  # noqa: E731
                 desc = {"impl": "gemm_f16", **pt, "group_size_m": args.group_size}
-            for _ in range(max(args.warmup, 3)):
-                run()
-            torch.cuda.synchronize(dev)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(steps):
-                run()
-            e1.record()
-            torch.cuda.synchronize(dev)
-            ms = e0.elapsed_time(e1) / steps
-            flops = 2.0 * w.M * w.N * w.K
+            runs.append((desc, run))
+        # points interleaved, each repetition after a rest, so that every point
+        # sees the same mix of power and clock states; the median is reported
+        times = [[] for _ in runs]
+        for _ in range(max(args.sweep_reps, 1)):
+            for i, (desc, run) in enumerate(runs):
+                time.sleep(args.sweep_rest)
+                for _ in range(max(args.warmup, 3)):
+                    run()
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(steps):
+                    run()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                times[i].append(e0.elapsed_time(e1) / steps)
+        flops = 2.0 * w.M * w.N * w.K
+        for (desc, _), t in zip(runs, times):
+            ms = statistics.median(t)
             print(json.dumps({"study": args.sweep, "workload": name, "M": w.M, "N": w.N, "K": w.K,
-                              **desc, "steps": steps, "ms_per_launch": ms,
-                              "tflops": flops / (ms * 1e-3) / 1e12, "status": sync_status()}),
+                              **desc, "steps": steps, "reps": len(t), "ms_per_launch": ms,
+                              "ms_per_launch_reps": t, "tflops": flops / (ms * 1e-3) / 1e12,
+                              "status": sync_status()}),
                   flush=True)
         del A, B, C
     return 0
