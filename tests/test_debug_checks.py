@@ -3,8 +3,8 @@ checks stand in for a sanitizer run. Every TMA copy's coordinates, every shared
 memory access of the wrappers, every TMEM load's columns and every plain store
 of C are checked; a failed check records GEMM_ERR_CHECK and skips the access.
 The cases cover every store path, both kernels, the alignment-class loader,
-split-K, 16-bit C, the dynamic schedule and the degenerate sizes, on integer
-inputs (exact)."""
+split-K, the split tail, 16-bit C, the dynamic schedule and the degenerate
+sizes, on integer inputs (exact)."""
 import json
 import os
 import subprocess
@@ -66,6 +66,8 @@ case("row-major order", 600, 700, 256, grouped=False)
 case("cross-tile off", 600, 700, 256, cross_tile=False)
 case("dynamic units", 2304, 2560, 640, dynamic=True)
 case("dynamic units, C view", 700, 513, 128, c=(520, 0), dynamic=True)
+case("split tail", 2304, 2560, 1280, tail_split=True)
+case("split tail, fp16 C", 700, 1200, 1100, dtype=torch.float16, tail_split=True)
 
 A0 = draw(512, 2048, "int", 90)
 B0 = draw(2048, 304, "int", 91)
@@ -94,7 +96,7 @@ def test_checked_library_finds_no_bad_access_and_reports_a_failed_check():
     assert res["library"].endswith("libgemm_f16_debug.so")
     bad = [c for c in res["cases"] if c["status"] != 0 or not c["exact"]]
     assert not bad, (bad, r.stderr[-2000:])
-    assert len(res["cases"]) == 24
+    assert len(res["cases"]) == 26
     # the reporting path works: one failing check -> GEMM_ERR_CHECK, cleared by the read
     assert res["selftest_entry"] == 0
     assert res["selftest_status"] == 5
