@@ -121,7 +121,9 @@ typedef enum {
  * and rounds into C. Results are deterministic, but the tail tiles' sums are no
  * longer bit-identical to the unsplit order's; integer-valued inputs (every
  * partial sum exact) stay exact. Calls with this flag that overlap on the GPU
- * share the scratch and race: serialise them. Where the conditions above do
+ * share the scratch and race: serialise them. The first call on a device that
+ * splits a tail looks up the scratch's device address (kept once a lookup
+ * succeeds); make it before any stream capture. Where the conditions above do
  * not hold the flag has no effect.
  * GEMM_SCHED_NON_PERSISTENT launches one program per tile ([persistent]
  * "naive tiled matmul" grid); program p then computes tile_id p only, and
