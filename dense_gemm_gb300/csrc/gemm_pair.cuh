@@ -302,11 +302,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         }
     } else if (warp == 0) {
         // ============================================================ producer (both CTAs)
-        if (lane == 0) {
+        // The whole warp walks the stage sequence with warp-uniform values. Lane 0
+        // arms the barriers and makes the cluster-launch-control requests; the
+        // copies of a stage (A: one box, or two 64-wide chunks when M-major; B
+        // likewise) are issued by separate lanes in one instruction. One thread
+        // issuing them in series took a measurable share of each k-block
+        // (device-timed on GB300: 16384^2 x 4096 1.266 -> 1.237 ms, 8192^2 x 4096
+        // 328.5 -> 321.8 us).
+        {
             const uint64_t pol_ld = l2_policy_evict_last();
             uint32_t stage = 0, phase = 0, issued = 0;
             bool ok = true;
             int32_t it = 0;
+            const int na = p.a_mn ? pair::CTA_M / MN_CHUNK : 1;  // copies of A per stage
+            const int nb = p.b_mn ? pair::CTA_N / MN_CHUNK : 1;  // copies of B per stage
             // dynamic units: CTA 0 asks for the next cluster's cancellation one unit
             // ahead; the answer lands in both CTAs, whose producers each arm their own
             // barrier for it, read it and publish the unit into their CTA's ring
@@ -315,14 +324,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
             auto clc_resp = [&](uint32_t i) { return base + Lay::off_clc_resp + 16u * (i % pair::NCLC); };
             auto clc_bar = [&](uint32_t i) { return bar0 + 8u * (Lay::clc_bar0 + i % pair::NCLC); };
             auto request = [&] {  // CTA 0
-                mbar_arrive_expect_tx(clc_bar(requested), 16);
-                clc_try_cancel_all(clc_resp(requested), clc_bar(requested));
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(clc_bar(requested), 16);
+                    clc_try_cancel_all(clc_resp(requested), clc_bar(requested));
+                }
                 ++requested;
             };
             auto publish = [&](uint32_t k, int32_t id) {  // unit number k >= 1 -> ring entry k - 1
-                const uint32_t q = (k - 1) % pair::QDEPTH;
-                st_shared_s32(qids + 4u * q, id);
-                mbar_arrive(qfull_bar(q));
+                if (lane == 0) {
+                    const uint32_t q = (k - 1) % pair::QDEPTH;
+                    st_shared_s32(qids + 4u * q, id);
+                    mbar_arrive(qfull_bar(q));
+                }
             };
             if (dyn && rank == 0) request();
             for (int32_t u = pair_id; ok && (!kDyn || u >= 0) && u < p.num_units; ++it) {
@@ -337,53 +350,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 tile_coords(tile, p.sched, tm, tn);
                 if (!p.cross_tile && it > 0) {
                     const int32_t j = it - 1;  // this CTA's epilogue has drained unit j
-                    if (!mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, mbar_wait(tdone_bar(j & 1), (j >> 1) & 1, p.wait))) {
+                        ok = false;
+                        break;
+                    }
                 }
                 const int32_t m0 = tm * pair::TILE_M + int32_t(rank) * pair::CTA_M;
                 const int32_t n0 = tn * pair::TILE_N + int32_t(rank) * pair::CTA_N;
                 for (int32_t kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
+                    if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, p.wait))) {
+                        ok = false;
+                        break;
+                    }
                     if (p.stop_after > 0 && issued >= uint32_t(p.stop_after)) {  // self-test: nothing more
                         if (++stage == NST) { stage = 0; phase ^= 1u; }
                         continue;
                     }
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair::PAIR_TX_BYTES);
+                    if (lane == 0 && rank == 0) mbar_arrive_expect_tx(full_bar(stage), pair::PAIR_TX_BYTES);
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     const int32_t k0 = kb * BK;
-                    const uint32_t a_dst = sA + stage * pair::A_STAGE_BYTES;
-                    const uint32_t b_dst = sB + stage * pair::B_STAGE_BYTES;
-                    if (p.l2_mode & 2u) {  // operand tiles are re-read by other pairs: keep in L2
-                        if (!p.a_mn) {
-                            tma_load_2d_pair_hint(a_dst, &tmA, k0, m0, fb, pol_ld);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < pair::CTA_M / MN_CHUNK; ++c)
-                                tma_load_2d_pair_hint(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK,
-                                                      k0, fb, pol_ld);
-                        }
-                        if (!p.b_mn) {
-                            tma_load_2d_pair_hint(b_dst, &tmB, k0, n0, fb, pol_ld);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < pair::CTA_N / MN_CHUNK; ++c)
-                                tma_load_2d_pair_hint(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK,
-                                                      k0, fb, pol_ld);
-                        }
-                    } else {
-                        if (!p.a_mn) {
-                            tma_load_2d_pair(a_dst, &tmA, k0, m0, fb);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < pair::CTA_M / MN_CHUNK; ++c)
-                                tma_load_2d_pair(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK, k0, fb);
-                        }
-                        if (!p.b_mn) {
-                            tma_load_2d_pair(b_dst, &tmB, k0, n0, fb);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < pair::CTA_N / MN_CHUNK; ++c)
-                                tma_load_2d_pair(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK, k0, fb);
-                        }
+                    if (lane < na + nb) {  // lane: copy `lane` of A, or copy `lane - na` of B
+                        const bool is_a = lane < na;
+                        const int c = is_a ? lane : lane - na;
+                        const CUtensorMap *map = is_a ? &tmA : &tmB;
+                        const uint32_t dst = (is_a ? sA + stage * pair::A_STAGE_BYTES : sB + stage * pair::B_STAGE_BYTES) +
+                                             uint32_t(c) * MN_CHUNK_BYTES;
+                        const bool mn_major = (is_a ? p.a_mn : p.b_mn) != 0;
+                        const int32_t mn = (is_a ? m0 : n0) + c * MN_CHUNK;
+                        const int32_t x = mn_major ? mn : k0, y = mn_major ? k0 : mn;
+                        if (p.l2_mode & 2u)  // operand tiles are re-read by other pairs: keep in L2
+                            tma_load_2d_pair_hint(dst, map, x, y, fb, pol_ld);
+                        else
+                            tma_load_2d_pair(dst, map, x, y, fb);
                     }
                     ++issued;
                     if (++stage == NST) { stage = 0; phase ^= 1u; }
@@ -395,8 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 } else {
                     int32_t nx = -1;
                     if (!ended) {
-                        if (rank != 0) mbar_arrive_expect_tx(clc_bar(answered), 16);  // this CTA's copy
-                        if (!mbar_wait(clc_bar(answered), (answered / pair::NCLC) & 1u, p.wait)) {
+                        if (rank != 0 && lane == 0) mbar_arrive_expect_tx(clc_bar(answered), 16);  // this CTA's copy
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait(clc_bar(answered), (answered / pair::NCLC) & 1u, p.wait))) {
                             ok = false;
                             break;
                         }
@@ -410,22 +409,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                     u = nx;
                 }
             }
-            // no cancellation answer may still be on its way into shared memory
-            for (uint32_t i = answered; i < requested; ++i)
-                mbar_wait_slow(clc_bar(i), (i / pair::NCLC) & 1u, cleanup_wait(p.wait), false);
-            if (!ok) {
-                if (rank == 0) {
-                    // Let the copies counted on this CTA's barriers land before exiting.
-                    const uint32_t n = issued < NST ? issued : NST;
-                    for (uint32_t q = issued - n; q < issued; ++q)
-                        mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u,
-                                       cleanup_wait(p.wait), false);
-                } else {
-                    // The peer's copies count on CTA 0's barriers, which it cannot
-                    // wait on; give copies already issued time to land (each is a
-                    // 16 KiB L2/HBM read, microseconds at most).
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) {
+            if (lane == 0) {
+                // no cancellation answer may still be on its way into shared memory
+                for (uint32_t i = answered; i < requested; ++i)
+                    mbar_wait_slow(clc_bar(i), (i / pair::NCLC) & 1u, cleanup_wait(p.wait), false);
+                if (!ok) {
+                    if (rank == 0) {
+                        // Let the copies counted on this CTA's barriers land before exiting.
+                        const uint32_t n = issued < NST ? issued : NST;
+                        for (uint32_t q = issued - n; q < issued; ++q)
+                            mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u,
+                                           cleanup_wait(p.wait), false);
+                    } else {
+                        // The peer's copies count on CTA 0's barriers, which it cannot
+                        // wait on; give copies already issued time to land (each is a
+                        // 16 KiB L2/HBM read, microseconds at most).
+                        const uint64_t t0 = global_timer_ns();
+                        while (global_timer_ns() - t0 < 200000ull) {
+                        }
                     }
                 }
             }
