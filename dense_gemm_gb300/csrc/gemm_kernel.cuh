@@ -801,51 +801,53 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
     if (warp < LOAD_WARPS) {
         // ============================================================ producer
         if constexpr (kTmaLoad) {
-            if (lane == 0) {
-                uint32_t stage = 0, phase = 0;
-                uint32_t issued = 0;
-                bool ok = true;
-                int32_t it = 0;
-                for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += grid, ++it) {
-                    int32_t tm, tn;
-                    tile_coords(tile, p.sched, tm, tn);
-                    if (!p.cross_tile && it > 0) {
-                        const int32_t j = it - 1;  // wait until tile j's accumulator is drained
-                        if (!mbar_wait(tempty_bar(j & 1), (j >> 1) & 1, p.wait)) { ok = false; break; }
-                    }
-                    const int32_t m0 = tm * BM, n0 = tn * BN;
-                    for (int32_t kb = 0; kb < num_kb; ++kb) {
-                        if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.wait)) { ok = false; break; }
-                        const uint32_t fb = full_bar(stage);
-                        mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
-                        const int32_t k0 = kb * BK;
-                        const uint32_t a_dst = sA + stage * A_STAGE_BYTES;
-                        const uint32_t b_dst = sB + stage * B_STAGE_BYTES;
-                        if (!p.a_mn) {
-                            tma_load_2d(a_dst, &tmA, k0, m0, fb);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < BM / MN_CHUNK; ++c)
-                                tma_load_2d(a_dst + c * MN_CHUNK_BYTES, &tmA, m0 + c * MN_CHUNK, k0, fb);
-                        }
-                        if (!p.b_mn) {
-                            tma_load_2d(b_dst, &tmB, k0, n0, fb);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < BN / MN_CHUNK; ++c)
-                                tma_load_2d(b_dst + c * MN_CHUNK_BYTES, &tmB, n0 + c * MN_CHUNK, k0, fb);
-                        }
-                        ++issued;
-                        if (++stage == NST) { stage = 0; phase ^= 1u; }
+            // The whole warp walks the stages; lane 0 arms the barrier and each
+            // of the stage's copies (A: 1 box or 2 chunks, B: 1 box or 4 chunks)
+            // is issued by its own lane, as in the CTA-pair kernel.
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued = 0;
+            bool ok = true;
+            int32_t it = 0;
+            const int na = p.a_mn ? BM / MN_CHUNK : 1;
+            const int nb = p.b_mn ? BN / MN_CHUNK : 1;
+            for (int32_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += grid, ++it) {
+                int32_t tm, tn;
+                tile_coords(tile, p.sched, tm, tn);
+                if (!p.cross_tile && it > 0) {
+                    const int32_t j = it - 1;  // wait until tile j's accumulator is drained
+                    if (!__all_sync(0xffffffffu, mbar_wait(tempty_bar(j & 1), (j >> 1) & 1, p.wait))) {
+                        ok = false;
+                        break;
                     }
                 }
-                if (!ok) {
-                    // Let the copies this thread started land before the CTA exits.
-                    const uint32_t n = issued < NST ? issued : NST;
-                    for (uint32_t q = issued - n; q < issued; ++q)
-                        mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u, cleanup_wait(p.wait),
-                                       false);
+                const int32_t m0 = tm * BM, n0 = tn * BN;
+                for (int32_t kb = 0; kb < num_kb; ++kb) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1u, p.wait))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    if (lane == 0) mbar_arrive_expect_tx(fb, A_STAGE_BYTES + B_STAGE_BYTES);
+                    const int32_t k0 = kb * BK;
+                    if (lane < na + nb) {  // lane: copy `lane` of A, or copy `lane - na` of B
+                        const bool is_a = lane < na;
+                        const int c = is_a ? lane : lane - na;
+                        const CUtensorMap *map = is_a ? &tmA : &tmB;
+                        const uint32_t dst =
+                            (is_a ? sA + stage * A_STAGE_BYTES : sB + stage * B_STAGE_BYTES) + uint32_t(c) * MN_CHUNK_BYTES;
+                        const bool mn_major = (is_a ? p.a_mn : p.b_mn) != 0;
+                        const int32_t mn = (is_a ? m0 : n0) + c * MN_CHUNK;
+                        tma_load_2d(dst, map, mn_major ? mn : k0, mn_major ? k0 : mn, fb);
+                    }
+                    ++issued;
+                    if (++stage == NST) { stage = 0; phase ^= 1u; }
                 }
+            }
+            if (!ok && lane == 0) {
+                // Let the copies this warp started land before the CTA exits.
+                const uint32_t n = issued < NST ? issued : NST;
+                for (uint32_t q = issued - n; q < issued; ++q)
+                    mbar_wait_slow(full_bar(q % NST), (q / NST) & 1u, cleanup_wait(p.wait), false);
             }
             __syncwarp();
         } else {
