@@ -70,7 +70,7 @@ def parse_args(argv=None):
                    help="repetitions of each study point (interleaved); the median is reported")
     p.add_argument("--sweep-rest", type=float, default=1.0,
                    help="seconds of rest before each timed study point")
-    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk",
+    p.add_argument("--sweep", choices=["order", "ksweep", "kernel", "persistence", "cublas", "splitk", "packed",
                                        "outdtype", "ragged", "schedule", "tail"],
                    default=None,
                    help="print one JSON line per point of a study instead of the bench line")
@@ -571,9 +571,13 @@ def run_sweep(args):
     schedule - the static pid + i*P tile stream vs GEMM_SCHED_DYNAMIC (cluster
                launch control) on 8192^2 x 4096, 16384^2 x 1024, 4000 x 5000 x 3000;
     tail - GEMM_SCHED_TAIL_SPLIT off/on (fp32 C, and fp16 C) with cuBLAS (fp16 C)
-           beside, on 8192^2 x 4096, 4000 x 5000 x 3000, 512^3 and the headline."""
+           beside, on 8192^2 x 4096, 4000 x 5000 x 3000, 512^3 and the headline;
+    packed - gemm_f16 vs gemm_f16_packed (operands copied onto 128-byte lines
+             first; with and without the split tail) on the ragged workloads and
+             8192^2 x 4100 (8200-byte rows)."""
     import torch
-    from dense_gemm_gb300 import gemm, gemm_splitk, splitk_workspace_size, sync_status
+    from dense_gemm_gb300 import (gemm, gemm_packed, gemm_splitk, packed_workspace_size, splitk_workspace_size,
+                                  sync_status)
     from dense_gemm_gb300.inputs import HEADLINE, WORKLOADS
 
     dev = torch.device("cuda", 0)
@@ -593,6 +597,9 @@ def run_sweep(args):
         names = ["square_8192x8192x4096", "ragged_4000x5000x3000", "square_512", HEADLINE]
         points = [dict(grouped=True, cross_tile=True, single_cta=False, tail_split=t) for t in (False, True)]
         points += [("out", torch.float16), ("out16_tail", torch.float16), "torch.matmul"]
+    elif args.sweep == "packed":
+        names = ["ragged_4000x5000x3000", "ragged_8191x8191x257", "unaligned_8192x8192x4100"]
+        points = [dict(grouped=True, cross_tile=True, single_cta=False), "packed", "packed_tail"]
     elif args.sweep == "outdtype":
         names = [HEADLINE, "ksweep_16384x16384x512"]
         points = [("out", torch.float32), ("out", torch.float16), ("out", torch.bfloat16)]
@@ -629,6 +636,15 @@ def run_sweep(args):
             elif pt == "torch.matmul":
                 run = lambda: torch.matmul(A, B)  # noqa: E731  (cuBLAS, fp16 output)
                 desc = {"impl": "torch.matmul (cuBLAS), fp16 output"}
+            elif pt in ("packed", "packed_tail"):
+                sam, sak = (max(x, 1) for x in A.stride())
+                sbk, sbn = (max(x, 1) for x in B.stride())
+                need = packed_workspace_size(w.M, w.N, w.K, sam, sak, sbk, sbn)
+                ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+                tail = pt == "packed_tail"
+                run = (lambda ws=ws, tail=tail:
+                       gemm_packed(A, B, C, workspace=ws, group_size_m=args.group_size, tail_split=tail))
+                desc = {"impl": "gemm_f16_packed", "tail_split": tail, "workspace_bytes": need}
             elif pt == "splitk":
                 need, used = splitk_workspace_size(w.M, w.N, w.K, 0)
                 ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)

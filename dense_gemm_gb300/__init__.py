@@ -10,5 +10,5 @@ from .binding import (  # noqa: F401
     sched_flags, gemm, gemm_raw, tile_map, get_config,
     sync_status, status_str, kernel_info, load_library, library_path, set_wait_timeout,
     gemm_from_host, selftest_wait_timeout, selftest_pair_abort, selftest_check, HostPipeline, gemm_splitk, splitk_workspace_size,
-    gemm_splitk_noalloc,
+    gemm_splitk_noalloc, gemm_packed, packed_workspace_size,
 )

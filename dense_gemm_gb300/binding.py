@@ -67,6 +67,12 @@ def load_library():
     lib.gemm_f16_splitk_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64,
                                             i64, i32, i32, u32, vp]
     lib.gemm_f16_splitk_noalloc.restype = ctypes.c_int
+    lib.gemm_f16_packed.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                    i32, u32, vp, u64, vp]
+    lib.gemm_f16_packed.restype = ctypes.c_int
+    lib.gemm_f16_packed_workspace_size.argtypes = [i64, i64, i64, i64, i64, i64, i64,
+                                                   ctypes.POINTER(u64)]
+    lib.gemm_f16_packed_workspace_size.restype = ctypes.c_int
     lib.gemm_f16_out.argtypes = [vp, vp, vp, i32, ctypes.c_float, i64, i64, i64, i64, i64, i64,
                                  i64, i64, i64, i32, u32, vp]
     lib.gemm_f16_out.restype = ctypes.c_int
@@ -183,6 +189,43 @@ def gemm(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
                                              _OUT_CODES[out.dtype], float(alpha), M, N, K, *strides,
                                              group_size_m, flags, _stream_handle(stream, dev))
             _check(st, "gemm_f16_out")
+    return out
+
+
+def packed_workspace_size(M: int, N: int, K: int, stride_am: int, stride_ak: int,
+                          stride_bk: int, stride_bn: int) -> int:
+    """Workspace bytes of gemm_f16_packed for these sizes and operand strides."""
+    b = ctypes.c_uint64()
+    _check(load_library().gemm_f16_packed_workspace_size(M, N, K, stride_am, stride_ak, stride_bk,
+                                                         stride_bn, ctypes.byref(b)),
+           "gemm_f16_packed_workspace_size")
+    return int(b.value)
+
+
+def gemm_packed(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor = None, *,
+                workspace: torch.Tensor = None, group_size_m: int = 8, grouped: bool = True,
+                cross_tile: bool = True, tail_split: bool = False, stream=None) -> torch.Tensor:
+    """C = A @ B through gemm_f16_packed: operands whose rows do not start on
+    128-byte boundaries are first copied into ``workspace`` (a CUDA tensor of at
+    least packed_workspace_size() bytes, allocated when omitted)."""
+    out = _check_operands(A, B, out)
+    M, K = A.shape
+    N = B.shape[1]
+    dev = A.device
+    sam, sak = (max(x, 1) for x in A.stride())
+    sbk, sbn = (max(x, 1) for x in B.stride())
+    scm, scn = (max(x, 1) for x in out.stride())
+    with torch.cuda.device(dev):
+        need = packed_workspace_size(M, N, K, sam, sak, sbk, sbn)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        _common_device(A, workspace)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        st = load_library().gemm_f16_packed(
+            A.data_ptr(), B.data_ptr(), out.data_ptr(), M, N, K, sam, sak, sbk, sbn, scm, scn,
+            group_size_m, sched_flags(grouped, cross_tile, tail_split=tail_split), workspace.data_ptr(),
+            ws_bytes, _stream_handle(stream, dev))
+    _check(st, "gemm_f16_packed")
     return out
 
 

@@ -363,11 +363,47 @@ struct SplitReq {
     int32_t stop_after = 0;  // failure-detection self-test (gemm_f16_selftest_pair_abort)
 };
 
+// Operand copies of one gemm_f16_packed call: the caller's workspace.
+struct PackReq {
+    bool enabled = false;
+    void *workspace = nullptr;
+    uint64_t workspace_bytes = 0;
+};
+
+// One operand's row layout: `rows` rows of `inner` contiguous elements, `ld`
+// elements apart (from the strides as gemm_impl classifies them).
+struct OperandRows {
+    int64_t rows, inner, ld;
+};
+
+OperandRows rows_of_a(int64_t M, int64_t K, int64_t stride_am, int64_t stride_ak) {
+    if (stride_ak == 1) return {M, K, stride_am};  // K-major
+    return {K, M, stride_ak};                      // M-major
+}
+
+OperandRows rows_of_b(int64_t N, int64_t K, int64_t stride_bk, int64_t stride_bn) {
+    if (stride_bn == 1) return {K, N, stride_bk};  // N-major
+    return {N, K, stride_bn};                      // K-major
+}
+
+// Elements per row of an operand's copy: whole 128-byte lines.
+int64_t packed_ld(int64_t inner) { return (inner + 63) / 64 * 64; }
+
+uint64_t packed_bytes(const OperandRows &o) { return uint64_t(o.rows) * uint64_t(packed_ld(o.inner)) * 2u; }
+
+uint64_t round256(uint64_t x) { return (x + 255u) / 256u * 256u; }
+
+// TMA reads every 64-element row of a K-block as one whole 128-byte line only
+// when the base and the row stride are multiples of 128 bytes.
+bool rows_on_lines(const void *p, const OperandRows &o) {
+    return (reinterpret_cast<uintptr_t>(p) & 127u) == 0 && (o.ld * 2) % 128 == 0 && o.ld >= o.inner;
+}
+
 gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                         int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
                         int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
                         uint32_t schedule_flags, gemm_stream_t stream_, const SplitReq &sk,
-                        uint32_t out_dtype = GEMM_OUT_F32, float alpha = 1.0f) {
+                        uint32_t out_dtype = GEMM_OUT_F32, float alpha = 1.0f, const PackReq &pk = PackReq()) {
     if (out_dtype > GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
     const int esize = out_dtype == GEMM_OUT_F32 ? 4 : 2;
     // ---- validation (no GPU work before this point)
@@ -381,12 +417,24 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     if (grouped && group_size_m < 1) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return GEMM_ERR_INVALID_ARG;
+    if (((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u) ||
+        (reinterpret_cast<uintptr_t>(C) & uintptr_t(esize - 1)))
+        return GEMM_ERR_INVALID_ARG;  // not aligned to the element size
     if (stride_cn != 1) return GEMM_ERR_UNSUPPORTED;
     if (M > 1 && stride_cm < N) return GEMM_ERR_INVALID_ARG;  // C rows would overlap
 
     const bool a_k = stride_ak == 1, a_m = !a_k && stride_am == 1;
     const bool b_n = stride_bn == 1, b_k = !b_n && stride_bk == 1;
     if (K > 0 && (!(a_k || a_m) || !(b_n || b_k))) return GEMM_ERR_UNSUPPORTED;
+
+    // gemm_f16_packed: the workspace holds both copies (checked before any GPU work)
+    const OperandRows pk_a = rows_of_a(M, K, stride_am, stride_ak);
+    const OperandRows pk_b = rows_of_b(N, K, stride_bk, stride_bn);
+    const uint64_t pk_off_b = round256(packed_bytes(pk_a));
+    if (pk.enabled && K > 0 &&
+        (pk.workspace == nullptr || (reinterpret_cast<uintptr_t>(pk.workspace) & 127u) ||
+         pk.workspace_bytes < pk_off_b + packed_bytes(pk_b)))
+        return GEMM_ERR_INVALID_ARG;
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev = 0;
@@ -401,6 +449,45 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
         const int blocks = int(blocks64 < 8 * int64_t(ds->num_sms) ? blocks64 : 8 * int64_t(ds->num_sms));
         zero_c_kernel<<<blocks, threads, 0, stream>>>(C, M, N, stride_cm, esize);
         return cudaGetLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    // ---- operand copies into whole 128-byte lines (gemm_f16_packed)
+    if (pk.enabled) {
+        const OperandRows &ra = pk_a, &rb = pk_b;
+        uint16_t *wa = static_cast<uint16_t *>(pk.workspace);
+        uint16_t *wb = reinterpret_cast<uint16_t *>(static_cast<unsigned char *>(pk.workspace) + pk_off_b);
+        auto job = [](const void *src, const OperandRows &o, uint16_t *dst, bool copy) {
+            PackJob j;
+            j.src = static_cast<const uint16_t *>(src);
+            j.dst = dst;
+            j.rows = o.rows;
+            j.inner = o.inner;
+            j.ld_src = o.ld;
+            j.ld_dst = packed_ld(o.inner);
+            j.gpr = (o.inner + 7) / 8;
+            j.granules = copy ? o.rows * j.gpr : 0;
+            return j;
+        };
+        const bool copy_a = !rows_on_lines(A, ra), copy_b = !rows_on_lines(B, rb);
+        const PackJob ja = job(A, ra, wa, copy_a), jb = job(B, rb, wb, copy_b);
+        const int64_t total = ja.granules + jb.granules;
+        if (total > 0) {
+            const int threads = 256;
+            const int64_t want = cdiv(total, threads);
+            const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
+            pack_rows_kernel<<<blocks, threads, 0, stream>>>(ja, jb);
+            if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+        }
+        if (copy_a) {
+            A = wa;
+            if (a_k) stride_am = packed_ld(ra.inner);
+            else stride_ak = packed_ld(ra.inner);
+        }
+        if (copy_b) {
+            B = wb;
+            if (b_n) stride_bk = packed_ld(rb.inner);
+            else stride_bn = packed_ld(rb.inner);
+        }
     }
 
     // ---- path selection per tensor
@@ -627,6 +714,33 @@ gemm_status_t gemm_f16_out(const void *A, const void *B, void *C, int32_t c_dtyp
     if (c_dtype < GEMM_OUT_F32 || c_dtype > GEMM_OUT_BF16) return GEMM_ERR_INVALID_ARG;
     return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
                      group_size_m, schedule_flags, stream, SplitReq(), uint32_t(c_dtype), alpha);
+}
+
+gemm_status_t gemm_f16_packed_workspace_size(int64_t M, int64_t N, int64_t K, int64_t stride_am,
+                                             int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                                             uint64_t *bytes) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_INVALID_ARG;
+    if (stride_am < 1 || stride_ak < 1 || stride_bk < 1 || stride_bn < 1) return GEMM_ERR_INVALID_ARG;
+    if (bytes) {
+        *bytes = 0;
+        if (M > 0 && N > 0 && K > 0)
+            *bytes = round256(packed_bytes(rows_of_a(M, K, stride_am, stride_ak))) +
+                     packed_bytes(rows_of_b(N, K, stride_bk, stride_bn));
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_f16_packed(const void *A, const void *B, float *C, int64_t M, int64_t N, int64_t K,
+                              int64_t stride_am, int64_t stride_ak, int64_t stride_bk, int64_t stride_bn,
+                              int64_t stride_cm, int64_t stride_cn, int32_t group_size_m,
+                              uint32_t schedule_flags, void *workspace, uint64_t workspace_bytes,
+                              gemm_stream_t stream) {
+    PackReq pk;
+    pk.enabled = true;
+    pk.workspace = workspace;
+    pk.workspace_bytes = workspace_bytes;
+    return gemm_impl(A, B, C, M, N, K, stride_am, stride_ak, stride_bk, stride_bn, stride_cm, stride_cn,
+                     group_size_m, schedule_flags, stream, SplitReq(), GEMM_OUT_F32, 1.0f, pk);
 }
 
 gemm_status_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int32_t splits,

@@ -1136,6 +1136,63 @@ __global__ void tail_reduce_kernel(const float *__restrict__ W, void *__restrict
     }
 }
 
+// ------------------------------------------------------------------ operand packing
+// One operand as `rows` rows of `inner` contiguous fp16 elements: element
+// (r, i) of the source at src[r * ld_src + i] (any 2-byte-aligned base, any
+// ld_src >= inner), of the copy at dst[r * ld_dst + i] (dst 128-byte aligned,
+// ld_dst a multiple of 64), so that every 64-element K-block row of the copy is
+// one whole 128-byte line.
+struct PackJob {
+    const uint16_t *src;
+    uint16_t *dst;
+    int64_t rows, inner, ld_src, ld_dst;
+    int64_t gpr;       // 16-byte granules of a copied row: cdiv(inner, 8)
+    int64_t granules;  // rows * gpr; 0 when the operand is not copied
+};
+
+// Copies A's and then B's granules, one 16-byte granule of the copy per thread
+// and step: the (one or two) aligned 16-byte source granules that hold its
+// elements are loaded and shifted into place; elements past `inner` are written
+// as zero. A source granule is read only when it holds an element of the row.
+__global__ void pack_rows_kernel(PackJob a, PackJob b) {
+    const int64_t total = a.granules + b.granules;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const bool second = e >= a.granules;
+        const PackJob &J = second ? b : a;
+        const int64_t f = second ? e - a.granules : e;
+        const int64_t r = f / J.gpr, j = f - r * J.gpr;
+        const int64_t i0 = 8 * j;
+        if (!G16_CHECK(r < J.rows && i0 < J.inner)) continue;
+        const int64_t left = J.inner - i0;
+        const uint32_t cnt = left < 8 ? uint32_t(left) : 8u;  // elements of this granule in the row
+        const uintptr_t s = reinterpret_cast<uintptr_t>(J.src + r * J.ld_src + i0);
+        const uintptr_t g0 = s & ~uintptr_t(15);
+        const uint32_t m = uint32_t(s - g0);  // even: fp16 elements
+        uint32_t w[8];
+        const uint4 lo = __ldg(reinterpret_cast<const uint4 *>(g0));
+        w[0] = lo.x, w[1] = lo.y, w[2] = lo.z, w[3] = lo.w;
+        if (m + 2 * cnt > 16) {  // the last elements lie in the next granule
+            const uint4 hi = __ldg(reinterpret_cast<const uint4 *>(g0 + 16));
+            w[4] = hi.x, w[5] = hi.y, w[6] = hi.z, w[7] = hi.w;
+        } else {
+            w[4] = w[5] = w[6] = w[7] = 0u;
+        }
+        uint32_t o[4];
+        window16(w, m, o);
+        if (cnt < 8) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (uint32_t(2 * t) >= cnt) o[t] = 0u;
+                else if (uint32_t(2 * t + 1) >= cnt) o[t] &= 0xffffu;
+            }
+        }
+        uint4 out;
+        out.x = o[0], out.y = o[1], out.z = o[2], out.w = o[3];
+        *reinterpret_cast<uint4 *>(J.dst + r * J.ld_dst + i0) = out;
+    }
+}
+
 // K == 0: C := 0 (the accumulator starts at zero and no K step adds to it).
 __global__ void zero_c_kernel(void *C, int64_t M, int64_t N, int64_t scm, int32_t esize) {
     const int64_t total = M * N;

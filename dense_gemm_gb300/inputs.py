@@ -104,6 +104,10 @@ WORKLOADS = {
     # headline's L2 behaviour (not one of the pages' shapes)
     "half_8192x16384x4096": Workload("half_8192x16384x4096", 8192, 16384, 4096, "normal", seed=1080,
                                      tags=("study",)),
+    # long K with 8200-byte rows of A and B (not 16-byte multiples): the case operand
+    # copies (gemm_f16_packed) are for (not one of the pages' shapes)
+    "unaligned_8192x8192x4100": Workload("unaligned_8192x8192x4100", 8192, 8192, 4100, "uniform",
+                                         b_layout="col", seed=1090, tags=("study",)),
     # few output tiles, long K: the case split-K is for (not one of the pages' shapes)
     "longk_1024x1024x32768": Workload("longk_1024x1024x32768", 1024, 1024, 32768, "uniform",
                                       seed=1070, tags=("study",)),

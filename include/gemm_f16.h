@@ -131,6 +131,8 @@ typedef enum {
  * counterpart on the pages) keeps programs resident like the persistent order
  * but hands out tiles as programs become free instead of tile_id = pid + i*grid;
  * the tile map itself is unchanged.
+ * A and B must be 2-byte aligned and C aligned to its element size, else
+ * GEMM_ERR_INVALID_ARG.
  * Sizes: M, N, K >= 0, each < 2^31. M == 0 or N == 0: nothing is done.
  * K == 0: C is set to 0.
  * Returns GEMM_OK once the work is enqueued.
@@ -170,6 +172,55 @@ gemm_status_t gemm_f16_out(const void *A, const void *B, void *C, int32_t c_dtyp
                            int64_t stride_cm, int64_t stride_cn,
                            int32_t group_size_m, uint32_t schedule_flags,
                            gemm_stream_t stream);
+
+/*
+ * gemm_f16_packed — gemm_f16 on copies of A and B whose rows start on
+ * 128-byte boundaries, made in a caller workspace. No counterpart on the pages
+ * (their operands are contiguous and aligned).
+ *
+ * The kernels read each operand as K-blocks of 64 elements: one 128-byte line
+ * per row. When an operand's base address or its row stride in bytes is not a
+ * multiple of 128, every such line straddles two lines of the L2 and costs two
+ * requests (measured on GB300: 4000 x 5000 x 3000 with row strides of 3000
+ * elements 106.6 us, with 3072 79.5 us); when it is not even a multiple of 16
+ * bytes the operand takes the alignment-class loader, several times slower at
+ * long K (8192^2 x 4100: 1042 us, 312 us on aligned copies). Each such operand
+ * is first copied, in its own orientation (a K-major operand stays K-major),
+ * into rows of round_up(inner, 64) elements at the start of the workspace (A)
+ * or 256-byte aligned after A's copy (B), by one copy kernel on `stream`; then
+ * gemm_f16 runs on the copies. An operand already on 128-byte lines is read in
+ * place. C is bit-identical to gemm_f16's (the same products, summed in the
+ * same order).
+ *
+ * Arguments, layouts and errors as gemm_f16, plus:
+ * workspace: DEVICE buffer owned by the caller, 128-byte aligned, of at least
+ *   gemm_f16_packed_workspace_size() bytes; NULL, misaligned or smaller ->
+ *   GEMM_ERR_INVALID_ARG (nothing is launched). The copies are left there; a
+ *   call that overlaps on the GPU must not use the same workspace.
+ * The copy reads whole aligned 16-byte granules of the source: it may read,
+ * and discard, bytes that share such a granule with an element of A or B,
+ * never others.
+ */
+gemm_status_t gemm_f16_packed(const void *A, const void *B, float *C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t stride_am, int64_t stride_ak,
+                              int64_t stride_bk, int64_t stride_bn,
+                              int64_t stride_cm, int64_t stride_cn,
+                              int32_t group_size_m, uint32_t schedule_flags,
+                              void *workspace, uint64_t workspace_bytes,
+                              gemm_stream_t stream);
+
+/*
+ * gemm_f16_packed_workspace_size — workspace bytes gemm_f16_packed needs for
+ * these sizes and operand strides (as gemm_f16's; they decide each operand's
+ * orientation): room for copies of both operands, whether or not a call ends
+ * up copying them. 0 when M, N or K is 0. Sizes or strides out of range ->
+ * GEMM_ERR_INVALID_ARG. `bytes` may be NULL. Needs no device.
+ */
+gemm_status_t gemm_f16_packed_workspace_size(int64_t M, int64_t N, int64_t K,
+                                             int64_t stride_am, int64_t stride_ak,
+                                             int64_t stride_bk, int64_t stride_bn,
+                                             uint64_t *bytes);
 
 /*
  * gemm_f16_splitk — C = A @ B with the K dimension split across CTA pairs

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     names = declared_functions()
     assert "gemm_f16" in names and "gemm_f16_tile_map" in names
-    assert len(names) == 14, names
+    assert len(names) == 16, names
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -171,3 +171,33 @@ def test_binding_rejects_operands_on_different_devices():
     assert _common_device(a, a, torch.empty(2, 2)) == torch.device("cpu")
     with pytest.raises(ValueError, match="one CUDA device"):
         _common_device(a, torch.empty(2, 2, dtype=torch.float16, device="meta"), a)
+
+
+def test_packed_host_validation(lib):
+    """gemm_f16_packed checks its workspace before any GPU work; the size query
+    needs no device."""
+    import ctypes as C
+    b = C.c_uint64()
+    # A K-major 300 x 257 (rows of 320 once copied), B K-major 500 x 257
+    assert lib.gemm_f16_packed_workspace_size(300, 500, 257, 257, 1, 1, 257, C.byref(b)) == 0
+    a_bytes = (300 * 320 * 2 + 255) // 256 * 256
+    assert b.value == a_bytes + 500 * 320 * 2
+    # A M-major (rows are K = 64 rows of M = 100 -> 128), B N-major (64 rows of 70 -> 128)
+    assert lib.gemm_f16_packed_workspace_size(100, 70, 64, 1, 100, 70, 1, C.byref(b)) == 0
+    assert b.value == (64 * 128 * 2 + 255) // 256 * 256 + 64 * 128 * 2
+    assert lib.gemm_f16_packed_workspace_size(0, 70, 64, 1, 100, 70, 1, C.byref(b)) == 0 and b.value == 0
+    assert lib.gemm_f16_packed_workspace_size(-1, 70, 64, 1, 100, 70, 1, None) == 1
+    assert lib.gemm_f16_packed_workspace_size(4, 70, 64, 0, 100, 70, 1, None) == 1
+    args = (16, 16, 16, 4, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3)
+    need = (4 * 64 * 2 + 255) // 256 * 256 + 4 * 64 * 2
+    assert lib.gemm_f16_packed(*args, None, need, None) == 1        # no workspace
+    assert lib.gemm_f16_packed(*args, 256 + 16, need, None) == 1    # not 128-byte aligned
+    assert lib.gemm_f16_packed(*args, 256, need - 1, None) == 1     # too small
+    assert lib.gemm_f16_packed(16, 16, 16, 0, 4, 4, 4, 1, 4, 1, 4, 1, 8, 3, None, 0, None) == 0  # M == 0
+
+
+def test_element_alignment_validation(lib):
+    # fp16 operands at odd addresses, fp32 C not 4-byte aligned -> INVALID_ARG before any GPU work
+    assert _call(lib, A=17) == 1
+    assert _call(lib, B=33) == 1
+    assert _call(lib, C=18) == 1

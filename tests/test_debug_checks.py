@@ -3,8 +3,8 @@ checks stand in for a sanitizer run. Every TMA copy's coordinates, every shared
 memory access of the wrappers, every TMEM load's columns and every plain store
 of C are checked; a failed check records GEMM_ERR_CHECK and skips the access.
 The cases cover every store path, both kernels, the alignment-class loader,
-split-K, the split tail, 16-bit C, the dynamic schedule and the degenerate
-sizes, on integer inputs (exact)."""
+split-K, the split tail, 16-bit C, the dynamic schedule, the operand copies of
+gemm_f16_packed and the degenerate sizes, on integer inputs (exact)."""
 import json
 import os
 import subprocess
@@ -79,6 +79,15 @@ st = sync_status()
 out["cases"].append({"name": "split-K", "status": st,
                      "exact": bool(np.array_equal(C.double().cpu().numpy(), oracle.gemm(A0, B0)))})
 
+from dense_gemm_gb300 import gemm_packed
+for (M, N, K, la, lb) in [(300, 500, 257, ("row", 3, 1), ("col", 5, 3)), (130, 270, 136, ("col", 2, 1), ("row", 6, 5))]:
+    A0 = draw(M, K, "int", 92 + M)
+    B0 = draw(K, N, "int", 93 + N)
+    C = gemm_packed(dev(relayout(A0, la[0], pad=la[1], offset=la[2])), dev(relayout(B0, lb[0], pad=lb[1], offset=lb[2])))
+    st = sync_status()
+    out["cases"].append({"name": f"packed operands {M}x{N}x{K}", "status": st,
+                         "exact": bool(np.array_equal(C.double().cpu().numpy(), oracle.gemm(A0, B0)))})
+
 out["selftest_entry"] = selftest_check()
 out["selftest_status"] = sync_status()
 out["status_after"] = sync_status()
@@ -96,7 +105,7 @@ def test_checked_library_finds_no_bad_access_and_reports_a_failed_check():
     assert res["library"].endswith("libgemm_f16_debug.so")
     bad = [c for c in res["cases"] if c["status"] != 0 or not c["exact"]]
     assert not bad, (bad, r.stderr[-2000:])
-    assert len(res["cases"]) == 26
+    assert len(res["cases"]) == 28
     # the reporting path works: one failing check -> GEMM_ERR_CHECK, cleared by the read
     assert res["selftest_entry"] == 0
     assert res["selftest_status"] == 5
