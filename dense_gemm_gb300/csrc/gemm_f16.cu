@@ -57,9 +57,9 @@ cudaError_t set_smem_attr() {
                                 Layout<L>::smem_bytes);
 }
 
-template <bool L, bool S, bool D = false, bool T = false>
+template <bool L, bool S, bool D = false, bool T = false, bool K = false>
 cudaError_t set_pair_smem_attr() {
-    return cudaFuncSetAttribute(gemm_f16_pair<L, S, D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm_f16_pair<L, S, D, T, K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 pair::Layout<L>::smem_bytes);
 }
 
@@ -106,6 +106,8 @@ cudaError_t device_init(int dev, DeviceState **out) {
     if (e == cudaSuccess) e = set_pair_smem_attr<true, true, true>();
     if (e == cudaSuccess) e = set_pair_smem_attr<true, false, true>();
     if (e == cudaSuccess) e = set_pair_smem_attr<true, true, false, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<true, false, false, false, true>();
+    if (e == cudaSuccess) e = set_pair_smem_attr<false, false, false, false, true>();
     if (e != cudaSuccess) {
         (void)cudaGetLastError();  // not sticky: leave no error behind for the caller's next call
         return e;
@@ -223,6 +225,46 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtens
     else
         gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, w, p, cm);
     return cudaGetLastError();
+}
+
+// The CTA-pair kernel with C stored per row class (plain-store C, static order).
+template <bool L>
+cudaError_t launch_pair_class(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &w, const Params &p,
+                              const ClassMaps &cm, const CClassMaps &cc, int grid, cudaStream_t stream) {
+    constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
+    if constexpr (L) {
+        gemm_f16_pair<L, false, false, false, true><<<grid, threads, smem, stream>>>(a, b, w, w, p, cc);
+    } else {
+        ClassMapsAndC all;
+        std::memcpy(all.a, cm.a, sizeof(all.a));
+        std::memcpy(all.b, cm.b, sizeof(all.b));
+        std::memcpy(all.c, cc.c, sizeof(all.c));
+        gemm_f16_pair<L, false, false, false, true><<<grid, threads, smem, stream>>>(a, b, w, w, p, all);
+    }
+    return cudaGetLastError();
+}
+
+// Row classes of an fp32 C that TMA cannot store as one map (see
+// epilogue_tile_class): P classes by the row stride, one map each whose rows
+// begin at the 16-byte boundary below the row starts and whose inner extent
+// ends on a granule at or before column N. Returns P, or 0 if C does not take
+// class stores (too small, or a map is rejected).
+uint32_t encode_c_classes(CClassMaps *cc, void *C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t d = ldc % 4;
+    const uint32_t P = d == 0 ? 1u : d == 2 ? 2u : 4u;
+    if (M < int64_t(P) || N < 8 || (reinterpret_cast<uintptr_t>(C) & 3u)) return 0;
+    if (uint64_t(P) * uint64_t(ldc) * 4u >= (uint64_t(1) << 40)) return 0;
+    std::memset(cc, 0, sizeof(*cc));
+    for (uint32_t q = 0; q < P; ++q) {
+        const uintptr_t row = reinterpret_cast<uintptr_t>(C) + uint64_t(q) * uint64_t(ldc) * 4u;
+        const uint32_t m = uint32_t((row >> 2) & 3u);
+        const uint64_t inner = (uint64_t(N) + m) / 4u * 4u;
+        const uint64_t rows = (uint64_t(M) - q + P - 1) / P;
+        if (!encode_2d(&cc->c[q], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, reinterpret_cast<const void *>(row - 4u * m),
+                       inner, rows, uint64_t(P) * uint64_t(ldc) * 4u, EPI_COLS, 32u / P))
+            return 0;
+    }
+    return P;
 }
 
 void tile_shape(uint32_t flags, int *bm, int *bn) {
@@ -638,6 +680,11 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
         p.tail_kps = tp.kps;
         p.num_units = tp.first + tp.splits * tp.tiles;
     }
+    // fp32 C that TMA cannot store as one map: per row class (CTA pairs, static order)
+    CClassMaps cc;
+    std::memset(&cc, 0, sizeof(cc));
+    if (use_pair && !store_tma && !split && tp.splits <= 1 && !dynamic && out_dtype == GEMM_OUT_F32)
+        p.c_classes = encode_c_classes(&cc, C, M, N, stride_cm);
     const int grid_programs = int(p.num_units < programs ? p.num_units : programs);
     if (use_pair && int64_t(grid_programs) * 2 > kMaxDim) return GEMM_ERR_UNSUPPORTED;
     const int grid = use_pair ? 2 * grid_programs : grid_programs;
@@ -680,6 +727,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     } else if (dynamic) {
         e = store_tma ? launch_pair<true, true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
                       : launch_pair<true, false, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
+    } else if (use_pair && p.c_classes > 0) {
+        e = load_tma ? launch_pair_class<true>(tmA, tmB, tmW, p, cm, cc, grid, stream)
+                     : launch_pair_class<false>(tmA, tmB, tmW, p, cm, cc, grid, stream);
     } else if (use_pair) {
         if (load_tma)
             e = store_tma ? launch_pair<true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)
@@ -823,7 +873,7 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t flags, int32_t 
 
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *static_smem,
                                    int32_t *dynamic_smem, int32_t *threads) {
-    if (variant < 0 || variant > 10) return GEMM_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 12) return GEMM_ERR_INVALID_ARG;
     cudaFuncAttributes a;
     cudaError_t e;
     int thr, dyn;
@@ -838,7 +888,9 @@ gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs, int32_t *stat
         case 7: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
         case 8: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
         case 9: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
-        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        case 10: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, true, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        case 11: e = cudaFuncGetAttributes(&a, gemm_f16_pair<true, false, false, false, true>); thr = pair::Layout<true>::threads; dyn = pair::Layout<true>::smem_bytes; break;
+        default: e = cudaFuncGetAttributes(&a, gemm_f16_pair<false, false, false, false, true>); thr = pair::Layout<false>::threads; dyn = pair::Layout<false>::smem_bytes; break;
     }
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     if (regs) *regs = a.numRegs;

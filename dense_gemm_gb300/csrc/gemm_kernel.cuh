@@ -126,6 +126,30 @@ struct ClassMapsFor<true> {
     using type = NoClassMaps;
 };
 
+// CTA-pair kernel with C stored per row class (see epilogue_tile_class): the
+// maps of C's classes, beside those of A and B for predicated loads.
+constexpr int MAX_C_CLASSES = 4;
+struct CClassMaps {
+    CUtensorMap c[MAX_C_CLASSES];
+};
+struct ClassMapsAndC {
+    CUtensorMap a[MAX_CLASSES];
+    CUtensorMap b[MAX_CLASSES];
+    CUtensorMap c[MAX_C_CLASSES];
+};
+template <bool kTmaLoad, bool kClassStore>
+struct PairMapsFor {
+    using type = typename ClassMapsFor<kTmaLoad>::type;
+};
+template <>
+struct PairMapsFor<true, true> {
+    using type = CClassMaps;
+};
+template <>
+struct PairMapsFor<false, true> {
+    using type = ClassMapsAndC;
+};
+
 __host__ __device__ constexpr int load_warps(bool tma_load) { return tma_load ? 1 : PRED_LOAD_WARPS; }
 __host__ __device__ constexpr int cta_threads(bool tma_load) {
     return (load_warps(tma_load) + 1 + EPI_WARPS) * 32;
@@ -277,6 +301,7 @@ struct Params {
     uint32_t cls_lh[2];
     uint32_t cls_mis[2];
     uint32_t cls_live[2];
+    uint32_t c_classes; // C stored per row class: number of classes P (1, 2 or 4), 0 otherwise
     float alpha;        // C = alpha * (A @ B)
     // Failure-detection self-test only (0 otherwise): the CTA-pair producers
     // issue no copies once they have issued this many stages, and keep waiting
@@ -407,7 +432,8 @@ __device__ __forceinline__ GroupShape group_shape(const Params &p, int op, int g
 // Starts the TMA copies of one group into ring slot `slot`; they complete on
 // `bar`. Lane 0 announces the byte count, then lane i < 64/h issues box i
 // (boxes of classes without rows are skipped and placed as zeros). Whole warp.
-__device__ __forceinline__ void issue_class_group(const Params &p, const ClassMaps &cm, const GroupShape &gs,
+template <typename Maps>
+__device__ __forceinline__ void issue_class_group(const Params &p, const Maps &cm, const GroupShape &gs,
                                                   int64_t k0, uint32_t slot, uint32_t bar, int lane) {
     const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
     const int nbox = GROUP_LINES >> gs.lh;
@@ -434,7 +460,8 @@ __device__ __forceinline__ void issue_class_group(const Params &p, const ClassMa
 // index within the group; box 0's lane announces the group's byte count on
 // `bar` first (ordered before the other boxes' issue by the caller's warp
 // convergence through __syncwarp). Boxes of classes without rows are skipped.
-__device__ __forceinline__ void issue_class_group_lanes(const Params &p, const ClassMaps &cm,
+template <typename Maps>
+__device__ __forceinline__ void issue_class_group_lanes(const Params &p, const Maps &cm,
                                                         const GroupShape &gs, int64_t k0, uint32_t slot,
                                                         uint32_t bar, int bi) {
     const uint32_t live = gs.op == 0 ? p.cls_live[0] : p.cls_live[1];
@@ -627,6 +654,127 @@ __device__ __forceinline__ void epilogue_tile(uint32_t t_row, int64_t row0, int6
             drained();
         store_chunk32<kTmaStore>(vb, row0, col_base + (c + 1) * EPI_COLS, p, tmC, stg, lane, split, ts);
     }
+}
+
+// ------------------------------------------------------------------ C stored per row class
+// fp32 C whose rows do not all start on a 16-byte boundary (and whose base and
+// row stride are multiples of 4 bytes): row i starts m_i floats (0..3) into a
+// granule, and rows with the same i mod P (P = 1, 2 or 4, from the row stride)
+// share m. Class q (rows q, q + P, ...) has a tensor map whose rows begin at the
+// granule boundary below each row start, so map column x is C column x - m_q;
+// its inner extent ends on a granule at or before column N, so no store reaches
+// past a row. A warp's 32 rows hold 32 / P rows of each class; lane l's row goes
+// to staging row (l % P) * (32 / P) + l / P, so that each class is one box.
+// Per warp column range [col0, end):
+//  * first chunk: the box at map column col0 + 4 (m > 0) holds C columns
+//    [col0 + d, col0 + d + 32), d = 4 - m: this chunk from column d on and the
+//    next chunk's first d values; columns [col0, col0 + d) go out as plain
+//    stores (m = 0: the box at col0, nothing plain);
+//  * chunk k > 0: the box at map column col0_k holds C columns [col0_k - m,
+//    col0_k - m + 32): the last m values of chunk k - 1, carried in registers,
+//    then the first 32 - m of chunk k. The one granule it shares with the first
+//    chunk's box is written twice with the same values;
+//  * columns [end - m, end), the carry after the last chunk: plain stores.
+// Units that reach C's last column use the plain path throughout.
+
+// This lane's row offset inside its 16-byte granule, in floats.
+__device__ __forceinline__ uint32_t row_misalignment(const Params &p, int64_t row) {
+    return (uint32_t(reinterpret_cast<uintptr_t>(p.C) >> 2) + uint32_t(uint64_t(row) * uint64_t(p.scm))) & 3u;
+}
+
+// o[t] = e(t + s) for t = 0..31, s = 0..3, e(i) a run of 35 values: two select
+// steps on the bits of s (whole registers only; s is uniform per lane).
+template <typename E>
+__device__ __forceinline__ void shift_run(E e, uint32_t s, uint32_t (&o)[32]) {
+    const bool b1 = (s & 1u) != 0, b2 = (s & 2u) != 0;
+    uint32_t y[34];  // y[i] = e(i + (s & 1)), i = 0 .. 33
+#pragma unroll
+    for (int i = 0; i < 34; ++i) y[i] = b1 ? e(i + 1) : e(i);
+#pragma unroll
+    for (int t = 0; t < 32; ++t) o[t] = b2 ? y[t + 2] : y[t];
+}
+
+template <typename Drained>
+__device__ __forceinline__ void epilogue_tile_class(uint32_t t_row, int64_t row0, int64_t col_base, int c0, int n,
+                                                    const Params &p, const CUtensorMap *cmaps, uint32_t stg,
+                                                    int lane, Drained drained) {
+    if (n == 0) {
+        drained();
+        return;
+    }
+    const uint32_t P = p.c_classes;
+    const uint32_t rpc = 32u / P;  // rows of each class in the warp's 32
+    const uint32_t m = row_misalignment(p, row0 + lane);
+    const uint32_t srow = (uint32_t(lane) % P) * rpc + uint32_t(lane) / P;
+    const bool row_ok = row0 + lane < p.M;
+    float *row_ptr = p.C + (row0 + lane) * p.scm;
+    uint32_t carry[3] = {0u, 0u, 0u};
+    auto scale = [&](uint32_t x) { return __float_as_uint(p.alpha * __uint_as_float(x)); };
+    // stage o (this lane's row of the boxes), then one box store per class
+    auto put = [&](const uint32_t (&o)[32], int32_t x) {
+        if (lane < int(P)) bulk_wait_group_read<0>();  // the buffer's previous stores have read it
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            st_shared_v4(stg + swz128(srow, u), o[4 * u], o[4 * u + 1], o[4 * u + 2], o[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane < int(P)) {  // lane q's row is of class q
+            tma_store_2d_hint(&cmaps[lane], stg + uint32_t(lane) * rpc * 128u, x, int32_t(row0 / P),
+                              l2_policy_evict_first());
+            bulk_commit_group();
+        }
+    };
+    auto emit = [&](uint32_t (&v)[32], int c, const uint32_t (*next)[32]) {
+        const int64_t col0 = col_base + int64_t(c) * EPI_COLS;
+        if (p.alpha != 1.0f) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = scale(v[i]);
+        }
+        uint32_t o[32];
+        if (next != nullptr) {  // the range's first chunk
+            const uint32_t d = (4u - m) & 3u;
+            uint32_t nx[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) nx[i] = p.alpha != 1.0f ? scale((*next)[i]) : (*next)[i];
+#pragma unroll
+            for (int i = 0; i < 3; ++i)
+                if (row_ok && uint32_t(i) < d && G16_CHECK(col0 + i < p.N)) row_ptr[col0 + i] = __uint_as_float(v[i]);
+            shift_run([&](int i) -> uint32_t { return i < 32 ? v[i] : nx[i - 32]; }, d, o);
+            put(o, int32_t(col0) + (m != 0 ? 4 : 0));
+        } else {
+            shift_run([&](int i) -> uint32_t { return i < 3 ? carry[i] : v[i - 3]; }, 3u - m, o);
+            put(o, int32_t(col0));
+        }
+        carry[0] = v[29];
+        carry[1] = v[30];
+        carry[2] = v[31];
+    };
+    uint32_t va[32], vb[32];
+    tmem_ld_32x32b_x32(t_row + c0 * EPI_COLS, va);
+#pragma unroll 1
+    for (int c = c0; c < c0 + n; c += 2) {
+        tmem_ld_wait();
+        tmem_ld_32x32b_x32(t_row + (c + 1) * EPI_COLS, vb);
+        if (c == c0) {
+            tmem_ld_wait();  // the first chunk's box takes the next chunk's first values
+            emit(va, c, &vb);
+        } else {
+            emit(va, c, nullptr);
+        }
+        tmem_ld_wait();
+        if (c + 2 < c0 + n)
+            tmem_ld_32x32b_x32(t_row + (c + 2) * EPI_COLS, va);
+        else
+            drained();
+        emit(vb, c + 1, nullptr);
+    }
+    // the carry of the last chunk: columns [end - m, end)
+    const int64_t end = col_base + int64_t(c0 + n) * EPI_COLS;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (row_ok && uint32_t(3 - i) <= m && G16_CHECK(end - 3 + i < p.N))
+            row_ptr[end - 3 + i] = __uint_as_float(carry[i]);
 }
 
 // Two fp32 values -> one 32-bit word of two 16-bit values (lo in the low half),

@@ -28,6 +28,8 @@
 // cluster-scope arrival to CTA 0 (a release at cluster scope costs a loader
 // warp 1000-3500 cycles; measured with clock64 timestamps).
 #pragma once
+#include <type_traits>
+
 #include "gemm_kernel.cuh"
 
 namespace g16 {
@@ -93,18 +95,30 @@ constexpr int SMEM_BYTES = Layout<true>::smem_bytes;
 constexpr int THREADS = Layout<true>::threads;
 }  // namespace pair
 
+// C's class maps of a kernel's map parameter (nullptr where it holds none).
+template <typename Maps>
+__device__ __forceinline__ const CUtensorMap *cm_c(const Maps &m) {
+    if constexpr (std::is_same_v<Maps, CClassMaps> || std::is_same_v<Maps, ClassMapsAndC>)
+        return m.c;
+    else
+        return nullptr;
+}
+
 // kDyn: units handed out by cluster launch control (TMA loads only); a
 // separate instantiation, so the static schedule carries none of its code.
 // kTail (TMA loads and stores, static schedule): the tiles of a last, partial
 // round are split along K across the programs that round would leave idle;
 // their fp32 partial tiles go to the scratch described by tmW, and a second
 // kernel sums them into C.
-template <bool kTmaLoad, bool kTmaStore, bool kDyn = false, bool kTail = false>
+// kClassStore (static schedule, fp32 C whose rows are not all 16-byte aligned):
+// C goes out per row class through the maps in cm.c (epilogue_tile_class).
+template <bool kTmaLoad, bool kTmaStore, bool kDyn = false, bool kTail = false, bool kClassStore = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoad>::threads, 1)
     gemm_f16_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
-                  const Params p, const __grid_constant__ typename ClassMapsFor<kTmaLoad>::type cm) {
+                  const Params p, const __grid_constant__ typename PairMapsFor<kTmaLoad, kClassStore>::type cm) {
     static_assert(!kTail || (kTmaLoad && kTmaStore && !kDyn), "split tail: TMA loads and stores, static stream");
+    static_assert(!kClassStore || (!kTmaStore && !kDyn && !kTail), "class stores: plain-store C, static stream");
     using Lay = pair::Layout<kTmaLoad>;
     constexpr int NST = Lay::stages;
     constexpr int LOAD_WARPS = Lay::load_warps;
@@ -170,6 +184,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         }
     }
     if (kTmaStore && warp == EPI_WARP0 && lane == 0) prefetch_tensormap(&tmC);
+    if constexpr (kClassStore) {
+        if (warp == EPI_WARP0 && lane < int(p.c_classes)) prefetch_tensormap(&cm_c(cm)[lane]);
+    }
     tc_fence_before();
     cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
@@ -560,7 +577,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, 0, &ts);
             } else if (p.out_dtype == 0 || p.splits > 1) {  // split-K partials are fp32
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS32, c0, n);
-                epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split);
+                if (kClassStore && col_base + pair::TILE_N <= p.N) {
+                    epilogue_tile_class(t_row, row0, col_base, c0, n, p, cm_c(cm), stg, lane, release);
+                } else {
+                    if (kClassStore) {  // the plain path reuses the buffer the class stores may still read
+                        if (lane < int(p.c_classes)) bulk_wait_group_read<0>();
+                        __syncwarp();
+                    }
+                    epilogue_tile<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release, split);
+                }
             } else {
                 epilogue_chunks(unit_kb, last, half, EPI_CHUNKS16, c0, n);
                 epilogue_tile16<kTmaStore>(t_row, row0, col_base, c0, n, p, &tmC, stg, lane, release);
@@ -571,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 u += num_pairs;
             }
         }
-        if (kTmaStore && lane == 0) bulk_wait_group<0>();
+        if ((kTmaStore && lane == 0) || (kClassStore && lane < int(p.c_classes))) bulk_wait_group<0>();
         __syncwarp();
     }
 

@@ -100,7 +100,15 @@ typedef enum {
  * (e.g. K = 257 row-major) through a predicated load/store path with the same
  * results. C also needs N to be a multiple of 4 for TMA stores (a clipped TMA
  * store writes whole 16-byte granules; the plain path writes exactly the M x N
- * elements). On that path the rows of A and B are copied per alignment class
+ * elements). An fp32 C that fails these conditions (rows not all 16-byte
+ * aligned, or N not a multiple of 4) is still stored mostly through TMA by the
+ * CTA-pair kernel (static order, N >= 8, a row in every class): rows that share their offset
+ * in a 16-byte granule form a class with a tensor map of its own whose rows
+ * end on a granule at or before column N, each row's values are shifted in
+ * registers so that every box starts on a granule, and the at most 3 leading
+ * and 3 trailing values of each row segment outside those boxes, and tiles
+ * that reach column N, are written with plain stores: only the M x N elements
+ * are written. On the predicated path the rows of A and B are copied per alignment class
  * (rows whose start shares its offset in a 16-byte granule), from the granule
  * boundary below each row start: it may read, and discard, bytes that share
  * an aligned 16-byte granule with an element of A or B, never others. If the
@@ -335,7 +343,9 @@ gemm_status_t gemm_f16_get_config(int64_t M, int64_t N, uint32_t schedule_flags,
  * 3 = predicated loads + predicated store. CTA-pair tiles, in the same
  * order: 4, 5, 6, 7; with GEMM_SCHED_DYNAMIC (TMA loads): 8 = TMA store,
  * 9 = predicated store; 10 = the CTA-pair kernel with a split tail
- * (GEMM_SCHED_TAIL_SPLIT). Outputs may be NULL. Needs a device.
+ * (GEMM_SCHED_TAIL_SPLIT); CTA pairs storing fp32 C per row class (C not
+ * TMA-storable as one map, see gemm_f16): 11 = TMA loads, 12 = predicated
+ * loads. Outputs may be NULL. Needs a device.
  */
 gemm_status_t gemm_f16_kernel_info(int32_t variant, int32_t *regs_per_thread,
                                    int32_t *static_smem, int32_t *dynamic_smem,

@@ -112,7 +112,7 @@ def test_product_library_has_no_device_checks(lib):
 
 def test_kernel_info_rejects_unknown_variant(lib):
     i32 = ctypes.POINTER(ctypes.c_int32)
-    assert lib.gemm_f16_kernel_info(11, i32(), i32(), i32(), i32()) == 1
+    assert lib.gemm_f16_kernel_info(13, i32(), i32(), i32(), i32()) == 1
     assert lib.gemm_f16_kernel_info(-1, i32(), i32(), i32(), i32()) == 1
 
 

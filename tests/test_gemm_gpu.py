@@ -155,6 +155,36 @@ def test_predicated_paths_bit_exact(case):
             assert np.isnan(buf[mask]).all(), name
 
 
+@pytest.mark.parametrize("M,ld,off,N", [(300, 1027, 0, 1027), (300, 1027, 3, 1025), (300, 1026, 1, 1026),
+                                        (300, 1025, 2, 1024), (300, 1028, 0, 1027), (300, 1028, 1, 1028),
+                                        (70, 8191, 0, 8191), (2600, 2051, 1, 2051), (2600, 2054, 2, 2053)])
+@pytest.mark.parametrize("K", [64, 800])
+def test_c_row_classes_bit_exact(M, ld, off, N, K):
+    """fp32 C whose rows are not all 16-byte aligned goes out per row class
+    (rows sharing their offset in a granule, one tensor map each) with the
+    values of each row shifted across chunk boundaries: every element exact,
+    every element outside C (row padding, before and after) keeps its NaN.
+    K = 64 splits a row block's chunks between two epilogue warps, K = 800
+    leaves them to one; M is not a multiple of 32. At 2600 rows there are more
+    tiles than CTA pairs, so warps go from class-stored tiles to the last tile
+    column (plain stores) and back."""
+    A = draw(M, K, "int", 470 + ld % 7)
+    B = draw(K, N, "int", 471 + N % 5)
+    want = oracle.gemm(A, B)
+    n = off + M * ld + 37
+    buf = torch.full((n,), float("nan"), device="cuda")
+    C = buf.as_strided((M, N), (ld, 1), off)
+    gemm(to_dev(A), to_dev(B), C)
+    torch.cuda.synchronize()
+    assert sync_status() == 0
+    assert np.array_equal(C.double().cpu().numpy(), want)
+    host = buf.cpu().numpy()
+    mask = np.ones(n, bool)
+    for i in range(M):
+        mask[off + i * ld: off + i * ld + N] = False
+    assert np.isnan(host[mask]).all(), f"{int((~np.isnan(host[mask])).sum())} values written outside C"
+
+
 OUT_TYPES = [(torch.float32, "f32"), (torch.float16, "f16"), (torch.bfloat16, "bf16")]
 
 
@@ -264,8 +294,9 @@ def test_invalid_arguments_raise():
 
 def test_kernel_resources():
     # warps: producer (1; predicated loads: 3 for one CTA, 4 + 1 issuer per CTA of a pair) + MMA + 8 epilogue
-    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448, 8: 320, 9: 320, 10: 320}
-    for v in range(11):
+    threads = {0: 320, 1: 320, 2: 384, 3: 384, 4: 320, 5: 320, 6: 448, 7: 448, 8: 320, 9: 320, 10: 320,
+               11: 320, 12: 448}
+    for v in range(13):
         info = kernel_info(v)
         assert info["dynamic_smem"] <= 232448 and info["regs_per_thread"] <= 255
         assert info["threads_per_cta"] == threads[v]
