@@ -294,6 +294,7 @@ struct Params {
     uint32_t l2_mode;   // bit 0: C stores evict-first; bit 1: A/B loads evict-last (pair kernel)
     uint32_t out_dtype; // C element type: 0 fp32, 1 fp16, 2 bf16 (nearest-even)
     uint32_t dynamic;   // units taken by cluster launch control (logged; the kernel instantiation decides)
+    uint32_t relay;     // CTA pairs with TMA loads: CTA 1's drained tiles reach CTA 0 through one relay arrive
     // predicated loads, per operand (0 = A, 1 = B): log2 of the class count P
     // and of the box height, each class's byte offset in its first granule (4
     // bits per class), and the classes that hold rows

@@ -156,7 +156,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(tfull_bar(a), 1);              // CTA 0's MMA commit (multicast)
-            mbar_init(tempty_bar(a), 2 * EPI_WARPS);  // every epilogue warp of both CTAs
+            // CTA 0's epilogue warps, and CTA 1's through its relay (or each of them)
+            mbar_init(tempty_bar(a), p.relay ? EPI_WARPS + 1 : 2 * EPI_WARPS);
             mbar_init(tdone_bar(a), EPI_WARPS);       // this CTA's epilogue warps
         }
         mbar_init(drain_bar, 1);
@@ -450,6 +451,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
+        if (kTmaLoad && rank == 1 && p.relay) {
+            // ======================================================== relay (CTA 1, TMA loads)
+            // Once all of this CTA's epilogue warps have drained a unit's
+            // accumulator (local arrivals), one release at cluster scope tells CTA
+            // 0's MMA warp, instead of one such arrival per epilogue warp (each
+            // costs its warp a cluster-scope fence on the drain's critical path).
+            int32_t it = 0;
+            for (int32_t u = pair_id; (!kDyn || u >= 0) && u < p.num_units; ++it) {
+                const uint32_t acc = it & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(tdone_bar(acc), (uint32_t(it) >> 1) & 1u, p.wait))) break;
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                __syncwarp();
+                if constexpr (kDyn) {
+                    if (!__all_sync(0xffffffffu, next_unit(uint32_t(it), u))) break;
+                } else {
+                    u += num_pairs;
+                }
+            }
+        }
         if (!kTmaLoad && rank == 1) {
             // ======================================================== relay (CTA 1, predicated loads)
             // Once this CTA's loader warps have filled a stage, one release at
@@ -559,7 +579,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(tdone_bar(acc));
-                    mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                    if (rank == 0)
+                        mbar_arrive(tempty_bar(acc));  // the MMA warp is in this CTA
+                    else if (!p.relay)
+                        mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
                 }
             };
             const int64_t col_base = int64_t(tn) * pair::TILE_N;
