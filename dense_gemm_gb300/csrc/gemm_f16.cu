@@ -656,11 +656,13 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
     // the others' units through cluster launch control (CTA pairs with TMA loads)
     const bool dynamic = (schedule_flags & GEMM_SCHED_DYNAMIC) && use_pair && load_tma;
     p.dynamic = dynamic ? 1u : 0u;
-    // CTA 1's epilogue warps report drained accumulators to CTA 0 through one
-    // relay arrive per unit (its MMA warp is idle with TMA loads): the per-warp
-    // cluster-scope arrivals it replaces cost 16384^2 x 512 253 -> 228 us and
-    // x 128 183 -> 167 us (device-timed on GB300, bit-identical C)
-    p.relay = (use_pair && load_tma) ? 1u : 0u;
+    // CTA 1's epilogue warps report a drained accumulator to CTA 0 with one
+    // cluster-scope arrive per unit: from CTA 1's MMA warp, idle with TMA loads,
+    // or (predicated loads) from the last of the warps to finish. The per-warp
+    // arrivals this replaces cost 16384^2 x 512 253 -> 228 us and x 128 183 ->
+    // 167 us with TMA loads, 8191^2 x 257 134 -> 133 us with predicated loads
+    // (device-timed on GB300, bit-identical C).
+    p.relay = use_pair ? 1u : 0u;
     const bool persistent = !(schedule_flags & GEMM_SCHED_NON_PERSISTENT) && !dynamic;
     const int programs = !persistent ? p.num_units
                          : use_pair  ? (load_tma ? ds->max_pairs : ds->max_pairs_pred)

@@ -140,6 +140,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     auto tdone_bar = [&](int a) { return bar0 + 8u * (2 * NST + 2 * NUM_ACC + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * NST + 3 * NUM_ACC);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::off_tmem_slot);
+    // per accumulator: CTA 1's epilogue warps that have drained it (predicated loads)
+    const uint32_t drained_ctr = base + Lay::off_tmem_slot + 8u;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -156,8 +158,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
         }
         for (int a = 0; a < NUM_ACC; ++a) {
             mbar_init(tfull_bar(a), 1);              // CTA 0's MMA commit (multicast)
-            // CTA 0's epilogue warps, and CTA 1's through its relay (or each of them)
+            // CTA 0's epilogue warps, and CTA 1's through one arrive (or each of them)
             mbar_init(tempty_bar(a), p.relay ? EPI_WARPS + 1 : 2 * EPI_WARPS);
+            st_shared_s32(drained_ctr + 4u * a, 0);
             mbar_init(tdone_bar(a), EPI_WARPS);       // this CTA's epilogue warps
         }
         mbar_init(drain_bar, 1);
@@ -579,10 +582,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(tdone_bar(acc));
-                    if (rank == 0)
+                    if (rank == 0) {
                         mbar_arrive(tempty_bar(acc));  // the MMA warp is in this CTA
-                    else if (!p.relay)
+                    } else if (!p.relay) {
                         mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                    } else if constexpr (!kTmaLoad) {
+                        // predicated loads (CTA 1's MMA warp relays the loaders' stages):
+                        // the last of this CTA's epilogue warps to drain the unit makes
+                        // the one cluster-scope arrive, having acquired the others' releases
+                        if ((atom_add_acq_rel_cta(drained_ctr + 4u * acc, 1u) + 1u) % uint32_t(EPI_WARPS) == 0)
+                            mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+                    }
                 }
             };
             const int64_t col_base = int64_t(tn) * pair::TILE_N;
