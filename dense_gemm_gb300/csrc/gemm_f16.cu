@@ -10,6 +10,7 @@
 #include <cstring>
 #include <mutex>
 #include <numeric>
+#include <utility>
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
@@ -205,15 +206,40 @@ bool tma_ok(const void *p, int64_t inner, int64_t outer_stride, int esize) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Launches a kernel of a GEMM call with programmatic stream serialization
+// allowed: its CTAs may be scheduled while the kernel before it on the stream
+// is finishing (once that kernel's CTAs have all called
+// griddepcontrol.launch_dependents, or ended), run their set-up, and wait in
+// griddepcontrol.wait, before their first global-memory access, until that
+// kernel has completed and its writes are visible. Memory ordering on the
+// stream is the same as for a plain launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), int grid, int threads, int smem, cudaStream_t stream,
+                              Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.blockDim = dim3(unsigned(threads), 1, 1);
+    cfg.dynamicSmemBytes = size_t(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e;
+}
+
 template <bool L, bool S>
 cudaError_t launch(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &c, const Params &p,
                    const ClassMaps &cm, int grid, cudaStream_t stream) {
     if constexpr (L)
-        gemm_f16_persistent<L, S><<<grid, cta_threads(L), Layout<L>::smem_bytes, stream>>>(a, b, c, p,
-                                                                                           NoClassMaps{});
+        return launch_overlapped(gemm_f16_persistent<L, S>, grid, cta_threads(L), Layout<L>::smem_bytes, stream, a, b,
+                                 c, p, NoClassMaps{});
     else
-        gemm_f16_persistent<L, S><<<grid, cta_threads(L), Layout<L>::smem_bytes, stream>>>(a, b, c, p, cm);
-    return cudaGetLastError();
+        return launch_overlapped(gemm_f16_persistent<L, S>, grid, cta_threads(L), Layout<L>::smem_bytes, stream, a, b,
+                                 c, p, cm);
 }
 
 template <bool L, bool S, bool D = false, bool T = false>
@@ -221,10 +247,10 @@ cudaError_t launch_pair(const CUtensorMap &a, const CUtensorMap &b, const CUtens
                         const Params &p, const ClassMaps &cm, int grid, cudaStream_t stream) {
     constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
     if constexpr (L)
-        gemm_f16_pair<L, S, D, T><<<grid, threads, smem, stream>>>(a, b, c, w, p, NoClassMaps{});
+        return launch_overlapped(gemm_f16_pair<L, S, D, T>, grid, threads, smem, stream, a, b, c, w, p,
+                                 NoClassMaps{});
     else
-        gemm_f16_pair<L, S><<<grid, threads, smem, stream>>>(a, b, c, w, p, cm);
-    return cudaGetLastError();
+        return launch_overlapped(gemm_f16_pair<L, S>, grid, threads, smem, stream, a, b, c, w, p, cm);
 }
 
 // The CTA-pair kernel with C stored per row class (plain-store C, static order).
@@ -233,15 +259,16 @@ cudaError_t launch_pair_class(const CUtensorMap &a, const CUtensorMap &b, const 
                               const ClassMaps &cm, const CClassMaps &cc, int grid, cudaStream_t stream) {
     constexpr int threads = pair::Layout<L>::threads, smem = pair::Layout<L>::smem_bytes;
     if constexpr (L) {
-        gemm_f16_pair<L, false, false, false, true><<<grid, threads, smem, stream>>>(a, b, w, w, p, cc);
+        return launch_overlapped(gemm_f16_pair<L, false, false, false, true>, grid, threads, smem, stream, a, b, w, w,
+                                 p, cc);
     } else {
         ClassMapsAndC all;
         std::memcpy(all.a, cm.a, sizeof(all.a));
         std::memcpy(all.b, cm.b, sizeof(all.b));
         std::memcpy(all.c, cc.c, sizeof(all.c));
-        gemm_f16_pair<L, false, false, false, true><<<grid, threads, smem, stream>>>(a, b, w, w, p, all);
+        return launch_overlapped(gemm_f16_pair<L, false, false, false, true>, grid, threads, smem, stream, a, b, w, w,
+                                 p, all);
     }
-    return cudaGetLastError();
 }
 
 // Row classes of an fp32 C that TMA cannot store as one map (see
@@ -517,8 +544,8 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
             const int threads = 256;
             const int64_t want = cdiv(total, threads);
             const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
-            pack_rows_kernel<<<blocks, threads, 0, stream>>>(ja, jb);
-            if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+            if (launch_overlapped(pack_rows_kernel, blocks, threads, 0, stream, ja, jb) != cudaSuccess)
+                return GEMM_ERR_CUDA;
         }
         if (copy_a) {
             A = wa;
@@ -715,9 +742,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
             const int threads = 256;
             const int64_t want = cdiv(quads, threads);
             const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
-            splitk_reduce_kernel<<<blocks, threads, 0, stream>>>(static_cast<const float *>(sk.workspace), C, M, N,
-                                                              sp.ldw, stride_cm, sp.splits, out_dtype, alpha);
-            e = cudaGetLastError();
+            e = launch_overlapped(splitk_reduce_kernel, blocks, threads, 0, stream,
+                                  static_cast<const float *>(sk.workspace), C, M, N, sp.ldw, stride_cm, sp.splits,
+                                  out_dtype, alpha);
         }
     } else if (tp.splits > 1) {
         e = launch_pair<true, true, false, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream);
@@ -726,10 +753,9 @@ gemm_status_t gemm_impl(const void *A, const void *B, void *C, int64_t M, int64_
             const int threads = 256;
             const int64_t want = cdiv(quads, threads);
             const int blocks = int(want < 8 * int64_t(ds->num_sms) ? want : 8 * int64_t(ds->num_sms));
-            tail_reduce_kernel<pair::TILE_M><<<blocks, threads, 0, stream>>>(
-                static_cast<const float *>(tail_ws), C, M, N, stride_cm, p.sched, tp.first, tp.tiles, tp.splits,
-                out_dtype, alpha);
-            e = cudaGetLastError();
+            e = launch_overlapped(tail_reduce_kernel<pair::TILE_M>, blocks, threads, 0, stream,
+                                  static_cast<const float *>(tail_ws), C, M, N, stride_cm, p.sched, tp.first,
+                                  tp.tiles, tp.splits, out_dtype, alpha);
         }
     } else if (dynamic) {
         e = store_tma ? launch_pair<true, true, true>(tmA, tmB, tmC, tmW, p, cm, grid, stream)

@@ -942,6 +942,10 @@ __global__ void __launch_bounds__(cta_threads(kTmaLoad), 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // The set-up above may overlap the end of the previous kernel on the
+    // stream; nothing below touches global memory before that kernel is done.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
 
     const int32_t grid = gridDim.x;
@@ -1178,6 +1182,8 @@ __global__ void tile_map_kernel(Sched s, int32_t num_tiles, int32_t *out) {
 __global__ void splitk_reduce_kernel(const float *__restrict__ W, void *__restrict__ Cv, int64_t M,
                                      int64_t N, int64_t ldw, int64_t scm, int32_t S,
                                      uint32_t out_dtype, float alpha) {
+    griddep_wait();  // the partial slices are the previous kernel's output
+    griddep_launch_dependents();
     const int64_t nq = (N + 3) / 4;
     const int64_t total = M * nq;
     const int64_t slice = M * ldw;
@@ -1233,6 +1239,8 @@ template <int TILE>
 __global__ void tail_reduce_kernel(const float *__restrict__ W, void *__restrict__ Cv, int64_t M, int64_t N,
                                    int64_t scm, Sched sched, int32_t first, int32_t tiles, int32_t S,
                                    uint32_t out_dtype, float alpha) {
+    griddep_wait();  // the partial tiles are the previous kernel's output
+    griddep_launch_dependents();
     constexpr int QUADS = TILE * TILE / 4;
     const int64_t total = int64_t(tiles) * QUADS;
     float *C = static_cast<float *>(Cv);
@@ -1304,6 +1312,8 @@ struct PackJob {
 // elements are loaded and shifted into place; elements past `inner` are written
 // as zero. A source granule is read only when it holds an element of the row.
 __global__ void pack_rows_kernel(PackJob a, PackJob b) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t total = a.granules + b.granules;
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
          e += int64_t(gridDim.x) * blockDim.x) {

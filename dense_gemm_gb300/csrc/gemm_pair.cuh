@@ -194,6 +194,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::Layout<kTmaLoa
     tc_fence_before();
     cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
+    // The set-up above may overlap the end of the previous kernel on the
+    // stream; nothing below touches global memory before that kernel is done.
+    griddep_wait();
+    griddep_launch_dependents();
     const uint32_t tmem_base = *tmem_slot;
     const int32_t num_kb = p.num_kb;
 

@@ -42,6 +42,16 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch. griddep_wait returns once every grid this
+// launch depends on (the kernel before it on the stream, when the launch
+// allowed programmatic serialization) has completed and its memory operations
+// are visible; without such a dependency it returns at once.
+// griddep_launch_dependents lets the next launch on the stream, if it allows
+// it, be scheduled before this grid has ended; that launch's own
+// griddep_wait still waits for this grid's completion.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

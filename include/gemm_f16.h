@@ -28,6 +28,15 @@
  *    call returns without waiting. Launch errors are returned; errors raised
  *    while the kernel runs (a bounded wait that ran out) are reported by
  *    gemm_f16_sync_status().
+ *  - Each kernel of a call is launched with programmatic stream serialization
+ *    allowed (programmatic dependent launch): its CTAs may be scheduled while
+ *    the kernel before it on the stream is finishing, and set themselves up
+ *    (barriers, tensor memory), but touch no global memory until that kernel
+ *    has completed and its writes are visible. Each kernel also lets the next
+ *    kernel on the stream be scheduled early; a kernel that is launched with
+ *    the same attribute must itself wait (griddepcontrol.wait) before it
+ *    reads this call's output, as one launched without it always does.
+ *    Ordering on the stream is that of plain launches.
  *  - Every entry point validates its arguments before touching the GPU and
  *    returns GEMM_ERR_INVALID_ARG / GEMM_ERR_UNSUPPORTED without side effects.
  *  - Thread safety: calls from several host threads are allowed; calls that
