@@ -5,7 +5,7 @@ Every kernel of a call is launched with programmatic stream serialization
 allowed: its CTAs may be scheduled while the kernel before it is finishing,
 and they wait (griddepcontrol.wait) before their first global-memory access.
 The chains below check that each link reads only its predecessor's finished
-output and writes nothing the predecessor still reads. With grids of 16-32
+output and writes nothing the predecessor still reads. With grids of 24-32
 CTA pairs on a 76-pair device, the next kernel's CTAs find free SMs at once,
 so a read taken before that wait would see the buffer's previous contents.
 
